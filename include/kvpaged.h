@@ -1,0 +1,189 @@
+/*
+ * kvpaged.h - C ABI of the GB300 paged KV-cache attention library (libkvpaged.so).
+ *
+ * The three calls are the data-parallel hot path of one attention layer of a
+ * nano-vLLM-style serving engine, as the engine's ModelRunner feeds it:
+ *
+ *   kv_store             scatter the step's new K/V rows into the paged cache
+ *   attn_prefill_varlen  varlen causal prefill over packed sequences, with a
+ *                        prefix cache (only the uncached suffix is queried)
+ *   attn_decode_paged    one query token per sequence over its paged history
+ *
+ * Sources: "nano-vLLM-1" (Senjl's Digital Garden), ModelRunner sections
+ * "3. KV cache 分配", "4. prefill 输入打包", "5. deocde 输入打包" and BlockManager
+ * section "3. 核心方法一：分配 (allocate)"; "Nano vLLM 解读（5）：解析 ModelRunner",
+ * sections on the KV cache tensor and "FlashAttention Kernel 函参准备";
+ * "【nano-vllm 学习】04 - 自顶向下的引擎调度层源码学习2", section
+ * "KV-Cache … 是什么？" (softmax(QK^T/sqrt(d_k))V with a causal mask).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - bf16 tensors are passed as pointers to their raw 16-bit patterns
+ *   (kvp_bf16).  Every pointer is a DEVICE pointer owned by the caller; the
+ *   library keeps no pointer after a call returns and allocates no memory
+ *   (scratch space, where a call needs it, is passed in as `workspace`).
+ * - Strides are in elements.  A "row" is one token: [heads, head_dim] contiguous.
+ * - One layer's caches: k_cache and v_cache are the views kv_cache[0, layer]
+ *   and kv_cache[1, layer] of the engine's [2, layers, num_blocks, block_size,
+ *   num_kv_heads, head_dim] tensor, i.e. each is [num_blocks, block_size,
+ *   num_kv_heads, head_dim] and contiguous.  Token slot s lives at block
+ *   s / block_size, offset s % block_size.
+ * - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *   default stream) and runs on the current CUDA device.
+ * - Return value: KVP_OK, or a negative KVP_ERR_* code when the call was
+ *   rejected before launch (nothing was enqueued) or the launch failed.
+ *   kvp_last_error() describes the last failure of the calling thread.
+ * - Contents of device-side metadata (slot values, block ids, context
+ *   lengths) are range-checked inside the kernels: an out-of-range value is
+ *   never dereferenced; the kernel records KVP_ERR_DEVICE_DATA in a device
+ *   status word that kvp_device_status() reads back.  Waits inside the kernels
+ *   are bounded; a wait that times out records KVP_ERR_DEVICE_TIMEOUT.
+ * - Head mapping (GQA): query head h reads kv head h / (num_heads /
+ *   num_kv_heads).
+ * - Arithmetic: bf16 inputs, fp32 accumulation, softmax in fp32 (base-2
+ *   exponentials with log2(e) folded into the scale), bf16 outputs.
+ */
+#ifndef KVPAGED_H
+#define KVPAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kvp_bf16;               /* raw bf16 bit pattern */
+typedef struct CUstream_st *kvp_stream_t; /* same type as cudaStream_t */
+
+enum {
+  KVP_OK = 0,
+  KVP_ERR_INVALID_ARG = -1,    /* null/misaligned pointer, bad size or stride */
+  KVP_ERR_UNSUPPORTED = -2,    /* shape outside what the kernels implement */
+  KVP_ERR_WORKSPACE = -3,      /* workspace missing or too small */
+  KVP_ERR_CUDA = -4,           /* a CUDA runtime/driver call failed */
+  KVP_ERR_DEVICE_TIMEOUT = -5, /* (device status) a bounded in-kernel wait expired */
+  KVP_ERR_DEVICE_DATA = -6     /* (device status) out-of-range slot / block id / length */
+};
+
+/* Message for the calling thread's last failed call ("" if none). */
+const char *kvp_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int kvp_version(void);
+
+/* Reads and clears the device status word of the current device (a blocking
+ * device-to-host read; it synchronizes with the device).  Returns KVP_OK,
+ * KVP_ERR_DEVICE_TIMEOUT, KVP_ERR_DEVICE_DATA, or KVP_ERR_CUDA if the read
+ * itself failed. */
+int kvp_device_status(void);
+
+/*
+ * kv_store - slot-mapped scatter of the step's new K/V rows.
+ *
+ * For every t < num_tokens with s = slot_mapping[t] >= 0:
+ *     k_cache[s / block_size][s % block_size][:][:] = k[t][:][:]
+ *     v_cache[s / block_size][s % block_size][:][:] = v[t][:][:]
+ * bit-exactly.  A slot of -1 (the engine's padding for CUDA-graph batches)
+ * writes nothing.  Source: "nano-vLLM-1" ModelRunner "4. prefill 输入打包" /
+ * "5. deocde 输入打包" (slot_mapping); "Nano vLLM 解读（5）" prepare_prefill.
+ *
+ *   k, v            [num_tokens, num_kv_heads, head_dim] bf16, row strides
+ *                   k_stride_tok / v_stride_tok (>= num_kv_heads*head_dim)
+ *   slot_mapping    [num_tokens] int32; values in [-1, num_blocks*block_size)
+ *   k_cache,v_cache [num_blocks, block_size, num_kv_heads, head_dim] bf16
+ * num_tokens == 0 is a no-op.  Slots must be distinct within one call (the
+ * engine never repeats one); a slot >= num_blocks*block_size or < -1 is
+ * skipped and flagged as KVP_ERR_DEVICE_DATA.
+ */
+int kv_store(const kvp_bf16 *k, const kvp_bf16 *v, int64_t k_stride_tok, int64_t v_stride_tok,
+             const int32_t *slot_mapping, int64_t num_tokens, kvp_bf16 *k_cache,
+             kvp_bf16 *v_cache, int64_t num_blocks, int block_size, int num_kv_heads,
+             int head_dim, kvp_stream_t stream);
+
+/*
+ * attn_prefill_varlen - causal attention over sequences packed back to back.
+ *
+ * Sequence b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and has
+ * k_len_b = cu_seqlens_k[b+1] - cu_seqlens_k[b] keys; its first
+ * c_b = k_len_b - q_len_b tokens are a cached prefix, so query row i is the
+ * token at absolute position c_b + i and attends to keys 0 .. c_b + i:
+ *     out[row, h] = sum_j softmax_j(q[row, h] . k_j * softmax_scale) v_j
+ * Source: "Nano vLLM 解读（5）" prepare_prefill (cu_seqlens_q/k, max_seqlen_q/k,
+ * block_tables only on a prefix hit); "nano-vLLM-1" "4. prefill 输入打包";
+ * "【nano-vllm 学习】04 …" causal mask.
+ *
+ *   q               [total_q, num_heads, head_dim] bf16, row stride q_stride_tok;
+ *                   total_q (= cu_seqlens_q[num_seqs]) bounds every read of q
+ *   block_tables    NULL: keys/values are the packed rows k, v
+ *                   [total_k, num_kv_heads, head_dim] (row stride
+ *                   kv_stride_tok; total_k = cu_seqlens_k[num_seqs]) and
+ *                   every q_len must equal its k_len;
+ *                   else [num_seqs, max_blocks_per_seq] int32 (right-padded
+ *                   with -1): keys/values are read from k_cache / v_cache
+ *                   through the block table (the step's own rows must already
+ *                   have been written there by kv_store)
+ *   cu_seqlens_q/k  [num_seqs + 1] int32 prefix sums, cu[0] = 0
+ *   max_seqlen_q/k  upper bounds of q_len / k_len over the batch
+ *   positions       optional [total_q] int64 (may be NULL); not read by the
+ *                   kernels (the causal offset is c_b + i)
+ *   out             [total_q, num_heads, head_dim] bf16, row stride out_stride_tok
+ * Supported: head_dim in {64, 128}; num_heads / num_kv_heads in {1, 2, 4, 8};
+ * block_size 16 * 2^k (16..4096).  q_len = 0 for a sequence is allowed (no
+ * rows).  No workspace.
+ */
+int attn_prefill_varlen(const kvp_bf16 *q, int64_t q_stride_tok, int64_t total_q,
+                        const kvp_bf16 *k, const kvp_bf16 *v, int64_t kv_stride_tok,
+                        int64_t total_k, const kvp_bf16 *k_cache,
+                        const kvp_bf16 *v_cache, int64_t num_blocks, int block_size,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                        int max_seqlen_q, int max_seqlen_k, int num_seqs,
+                        const int64_t *positions, int num_heads, int num_kv_heads, int head_dim,
+                        float softmax_scale, kvp_bf16 *out, int64_t out_stride_tok,
+                        kvp_stream_t stream);
+
+/*
+ * Bytes of device workspace attn_decode_paged needs for this shape on the
+ * current device (0 on error; see kvp_last_error).
+ */
+size_t attn_decode_workspace_size(int num_seqs, int num_heads, int head_dim,
+                                  int max_context_len, int block_size);
+
+/*
+ * attn_decode_paged - one query token per sequence over its paged history.
+ *
+ * Sequence b attends to its context_lens[b] tokens (the count includes the
+ * token being decoded, which kv_store has just written), token p being read at
+ * k_cache/v_cache[block_tables[b][p / block_size]][p % block_size]:
+ *     out[b, h] = sum_{p < context_lens[b]} softmax_p(q[b, h] . k_p * scale) v_p
+ * A sequence with context_lens[b] == 0 (the engine's padding rows) reads
+ * nothing and gets an all-zero output row.
+ * Source: "Nano vLLM 解读（5）" prepare_decode (context_lens, block_tables);
+ * "nano-vLLM-1" "5. deocde 输入打包".
+ *
+ *   q               [num_seqs, num_heads, head_dim] bf16, row stride q_stride_tok
+ *   block_tables    [num_seqs, max_blocks_per_seq] int32
+ *   context_lens    [num_seqs] int32, each <= max_context_len and
+ *                   <= max_blocks_per_seq * block_size
+ *   workspace       device scratch of at least attn_decode_workspace_size()
+ *                   bytes, 16-byte aligned; its contents need no
+ *                   initialisation and are garbage afterwards.  Two calls that
+ *                   run at the same time must not share a workspace.
+ *   out             [num_seqs, num_heads, head_dim] bf16, row stride out_stride_tok
+ * Supported: head_dim in {64, 128}; num_kv_heads in {1, 2, 4, 8};
+ * num_heads / num_kv_heads in {1, 2, 4, 8}; any block_size >= 1.
+ */
+int attn_decode_paged(const kvp_bf16 *q, int64_t q_stride_tok, const kvp_bf16 *k_cache,
+                      const kvp_bf16 *v_cache, int64_t num_blocks, int block_size,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, int num_seqs, int max_context_len,
+                      int num_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                      void *workspace, size_t workspace_bytes, kvp_bf16 *out,
+                      int64_t out_stride_tok, kvp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVPAGED_H */

@@ -1,0 +1,653 @@
+// attn_decode_paged: one query token per sequence over its paged KV history.
+//
+// Source: "Nano vLLM 解读（5）：解析 ModelRunner", prepare_decode (context_lens
+// counts the token being decoded; block_tables map logical to physical
+// blocks); "nano-vLLM-1" "5. deocde 输入打包"; attention itself is
+// softmax(q K^T * scale) V ("【nano-vllm 学习】04 …", "KV-Cache … 是什么？").
+//
+// Design (memory bound: every K/V byte of the batch is read exactly once).
+//
+// * Flat split over the whole batch.  The tokens of all sequences, laid end
+//   to end (T = sum context_lens), are cut into one contiguous chunk per CTA
+//   (ceil(T / CTAs)), and the grid is one persistent CTA per SM.  Every SM
+//   streams the same number of bytes whatever the length mix; a sequence cut
+//   by a chunk boundary leaves partial results (running max m, sum l, and the
+//   un-normalised accumulator) that a small merge kernel combines by
+//   log-sum-exp.  A sequence inside one chunk is finished in place.
+// * Each CTA reads all kv heads of a token at once: a token's K row for all
+//   heads is num_kv_heads * head_dim contiguous bf16 (2 KiB for 8 x 128), so
+//   a stage of up to 64 / num_kv_heads tokens of one physical block is one
+//   contiguous 1-D bulk copy for K and one for V (16 KiB each at 8 x 128).  A
+//   producer warp streams stages into a 6-deep shared-memory ring
+//   (cp.async.bulk + mbarrier transaction counts); it reads the block table as
+//   it goes, so the gather costs nothing beyond the copy addresses.
+// * Eight consumer warps; warp w serves kv head w % Hkv (and, when
+//   Hkv < 8, token subset w / Hkv).  A lane owns 1/8 of head_dim (two 16-byte
+//   chunks at head_dim 128) of one token; 4 tokens per pass.  q . k is an
+//   fp32 dot product over the lane's slice reduced over 8 lanes by shuffles,
+//   with q pre-scaled by softmax_scale * log2(e) so the softmax uses exp2.
+//   The running max is warp-uniform and updated once per stage.
+#include <cfloat>
+
+#include "kvp_device.cuh"
+
+namespace kvp {
+namespace {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kStages = 6;
+constexpr int kTokensAllHeads = 64;  // tokens * kv heads per stage
+
+// Row of one split partial in the workspace: accumulator[D], m, l, and two pad
+// floats so that every row starts on a 16-byte boundary (float4 stores).
+template <int D>
+__host__ __device__ constexpr int part_stride() {
+  return D + 4;
+}
+
+enum : int { F_NEW = 1, F_LAST = 2, F_ENTERED = 4, F_EXITS = 8, F_DONE = 16 };
+
+struct StageMeta {
+  int b;
+  int n;
+  int flags;
+  int pad;
+};
+
+struct DecodeArgs {
+  const uint16_t* q;
+  int64_t q_stride;
+  const uint16_t* k_cache;
+  const uint16_t* v_cache;
+  int64_t num_blocks;
+  int block_size;
+  const int32_t* block_tables;
+  int max_blocks;
+  const int32_t* ctx;
+  int num_seqs;
+  int num_heads;
+  int num_kv_heads;
+  float scale_log2;
+  float* part;     // [ctas][2][Hq][D + 4]: accumulator[D], m, l, pad
+  int* split_seq;  // [ctas]: sequence continuing into the next CTA, or -1
+  uint16_t* out;
+  int64_t out_stride;
+  int* status;
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ int clamp_len(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
+
+template <int D>
+__host__ __device__ constexpr size_t stage_half_bytes() {
+  return (size_t)kTokensAllHeads * D * sizeof(uint16_t);
+}
+
+// With 9 warps per CTA one SM sub-partition runs 3 of them, so a thread can
+// hold at most 168 registers.  When the scaled query slice of a lane (G * D / 8
+// floats) plus the accumulators would not fit, the query lives in shared
+// memory (per warp, fp32) and is read with broadcast loads.
+template <int D, int G>
+__host__ __device__ constexpr bool q_in_smem() {
+  return G * D >= 512;
+}
+
+template <int D, int G>
+__host__ __device__ constexpr size_t decode_smem_bytes() {
+  return 2 * kStages * stage_half_bytes<D>() + kStages * sizeof(StageMeta) +
+         (2 * kStages + 2 * kConsumerWarps) * sizeof(uint64_t) +
+         (size_t)kConsumerWarps * G * (D + 2) * sizeof(float) +
+         (q_in_smem<D, G>() ? (size_t)kConsumerWarps * G * D * sizeof(float) : 0);
+}
+
+// ---------------------------------------------------------------- producer
+
+template <int D>
+__device__ void decode_producer(const DecodeArgs& a, uint8_t* ringK, uint8_t* ringV,
+                                StageMeta* meta, uint64_t* full, uint64_t* empty) {
+  const int lane = threadIdx.x & 31;
+  const int Hkv = a.num_kv_heads;
+  const int cap = a.max_blocks * a.block_size;
+  const int P = gridDim.x;
+
+  // Total tokens of the batch (every CTA computes the same value).
+  long long tot = 0;
+  for (int i = lane; i < a.num_seqs; i += 32) {
+    const int c = a.ctx[i];
+    if (c < 0 || c > cap) record_error(a.status, KVP_ERR_DEVICE_DATA);
+    tot += clamp_len(c, cap);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  const long long chunk = (tot + P - 1) / P;
+  const long long start = (long long)blockIdx.x * chunk;
+  const long long end = start + chunk < tot ? start + chunk : tot;
+
+  // Rows of sequences with no context are zero (they read nothing).
+  for (int b = blockIdx.x; b < a.num_seqs; b += P) {
+    if (clamp_len(a.ctx[b], cap) != 0) continue;
+    uint4* o = reinterpret_cast<uint4*>(a.out + (int64_t)b * a.out_stride);
+    for (int i = lane; i < a.num_heads * D / 8; i += 32) o[i] = make_uint4(0, 0, 0, 0);
+  }
+
+  // First sequence overlapping [start, end): warp scan over context_lens.
+  int b0 = 0;
+  long long cum0 = 0;
+  if (start < end) {
+    long long run = 0;
+    for (int base = 0; base < a.num_seqs; base += 32) {
+      const int i = base + lane;
+      const long long c = i < a.num_seqs ? clamp_len(a.ctx[i], cap) : 0;
+      long long incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, i < a.num_seqs && run + incl > start);
+      if (hit) {
+        const int L = __ffs(hit) - 1;
+        b0 = base + L;
+        cum0 = run + __shfl_sync(0xffffffffu, incl - c, L);
+        break;
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  if (lane != 0) return;
+
+  a.split_seq[blockIdx.x] = -1;
+  const int T = kTokensAllHeads / Hkv;
+  const int64_t row_elems = (int64_t)Hkv * D;
+  int s = 0;
+  uint32_t ph = 0;
+  uint32_t issued = 0, issued_ph = 0;  // per stage: ever issued / parity of the last issue
+  bool ok = true;
+
+  long long pos = start, cum = cum0;
+  int b = b0;
+  while (ok && pos < end && b < a.num_seqs) {
+    const int L = clamp_len(a.ctx[b], cap);
+    if (L == 0) {
+      ++b;
+      continue;
+    }
+    const long long seq_end = cum + L;
+    const long long seg_end = end < seq_end ? end : seq_end;
+    int t = (int)(pos - cum);
+    const int t1 = (int)(seg_end - cum);
+    const int seg_flags = (pos > cum ? F_ENTERED : 0) | (seg_end < seq_end ? F_EXITS : 0);
+    bool first = true;
+    int cur_bi = -1, phys = 0;
+    while (t < t1) {
+      const int bi = t / a.block_size, off = t - bi * a.block_size;
+      int n = a.block_size - off;
+      if (n > T) n = T;
+      if (n > t1 - t) n = t1 - t;
+      if (bi != cur_bi) {
+        cur_bi = bi;
+        phys = a.block_tables[(int64_t)b * a.max_blocks + bi];
+        if (phys < 0 || phys >= a.num_blocks) {
+          record_error(a.status, KVP_ERR_DEVICE_DATA);
+          phys = 0;  // never dereference an out-of-range block
+        }
+      }
+      if (!mbar_wait(&empty[s], ph ^ 1u, a.status)) {
+        ok = false;
+        break;
+      }
+      meta[s].b = b;
+      meta[s].n = n;
+      meta[s].flags = (first ? F_NEW : 0) | (t + n == t1 ? F_LAST : 0) | seg_flags;
+      const uint32_t bytes = (uint32_t)(n * row_elems * sizeof(uint16_t));
+      mbar_arrive_expect_tx(&full[s], 2 * bytes);
+      const int64_t row0 = ((int64_t)phys * a.block_size + off) * row_elems;
+      bulk_g2s(ringK + (size_t)s * stage_half_bytes<D>(), a.k_cache + row0, bytes, &full[s]);
+      bulk_g2s(ringV + (size_t)s * stage_half_bytes<D>(), a.v_cache + row0, bytes, &full[s]);
+      issued |= 1u << s;
+      issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+      first = false;
+      t += n;
+      if (++s == kStages) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    if (seg_flags & F_EXITS) a.split_seq[blockIdx.x] = b;
+    pos = seg_end;
+    cum = seq_end;
+    ++b;
+  }
+  if (ok && mbar_wait(&empty[s], ph ^ 1u, a.status)) {
+    meta[s].flags = F_DONE;
+    mbar_arrive(&full[s]);
+    return;
+  }
+  // A wait expired: let every copy this CTA issued land before the CTA exits.
+  for (int i = 0; i < kStages; ++i)
+    if (issued >> i & 1u) mbar_wait(&full[i], issued_ph >> i & 1u, a.status);
+}
+
+// ---------------------------------------------------------------- consumers
+
+template <int D, int G>
+__device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const uint8_t* ringV,
+                                const StageMeta* meta, uint64_t* full, uint64_t* empty,
+                                uint64_t* xfull, uint64_t* xfree, float* xw, float* qs_all) {
+  constexpr int NCH = D / 64;  // 16-byte chunks of one row per lane
+  constexpr bool kQS = q_in_smem<D, G>();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hkv = a.num_kv_heads;
+  const int NS = kConsumerWarps / Hkv;
+  const int g = warp % Hkv, sub = warp / Hkv;
+  const int li = lane & 7, tg = lane >> 3;
+  const int row_elems = Hkv * D;
+
+  // Scaled query: registers, or this warp's [G][D] fp32 slice of shared memory.
+  float qf[kQS ? 1 : G][NCH][8];
+  float* qs = qs_all + (size_t)warp * G * D;
+  float acc[G][NCH][8];
+  float m[G], l[G];
+  int b = 0;
+  int s = 0;
+  uint32_t ph = 0;
+  int seg = 0;  // segments finished so far (same count in every warp)
+
+  while (true) {
+    if (!mbar_wait(&full[s], ph, a.status)) return;
+    const StageMeta md = meta[s];
+    if (md.flags & F_DONE) break;
+
+    if (md.flags & F_NEW) {
+      b = md.b;
+      const uint16_t* qrow = a.q + (int64_t)b * a.q_stride + (int64_t)g * G * D;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const uint4 u = *reinterpret_cast<const uint4*>(qrow + h * D + (c * 8 + li) * 8);
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+          if constexpr (kQS) {
+            if (tg == 0) {
+              float4* d4 = reinterpret_cast<float4*>(qs + h * D + (c * 8 + li) * 8);
+              d4[0] = make_float4(bf16lo(w[0]) * a.scale_log2, bf16hi(w[0]) * a.scale_log2,
+                                  bf16lo(w[1]) * a.scale_log2, bf16hi(w[1]) * a.scale_log2);
+              d4[1] = make_float4(bf16lo(w[2]) * a.scale_log2, bf16hi(w[2]) * a.scale_log2,
+                                  bf16lo(w[3]) * a.scale_log2, bf16hi(w[3]) * a.scale_log2);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              qf[h][c][2 * e] = bf16lo(w[e]) * a.scale_log2;
+              qf[h][c][2 * e + 1] = bf16hi(w[e]) * a.scale_log2;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[h][c][e] = 0.f;
+        }
+        m[h] = -INFINITY;
+        l[h] = 0.f;
+      }
+      if constexpr (kQS) __syncwarp();
+    }
+
+    const uint16_t* Ks = reinterpret_cast<const uint16_t*>(ringK + (size_t)s * stage_half_bytes<D>());
+    const uint16_t* Vs = reinterpret_cast<const uint16_t*>(ringV + (size_t)s * stage_half_bytes<D>());
+
+    // Scores of this warp's 2 x 4 tokens for its G query heads.
+    float sc[2][G];
+    bool valid[2];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const int tl = (p * NS + sub) * 4 + tg;
+      valid[p] = tl < md.n;
+      const uint4* kr = reinterpret_cast<const uint4*>(Ks + (size_t)tl * row_elems + g * D);
+      uint4 kv[NCH];
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) kv[c] = kr[c * 8 + li];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          const uint32_t w[4] = {kv[c].x, kv[c].y, kv[c].z, kv[c].w};
+          float qv[8];
+          if constexpr (kQS) {
+            const float4* q4 = reinterpret_cast<const float4*>(qs + h * D + (c * 8 + li) * 8);
+            const float4 a0 = q4[0], a1 = q4[1];
+            qv[0] = a0.x; qv[1] = a0.y; qv[2] = a0.z; qv[3] = a0.w;
+            qv[4] = a1.x; qv[5] = a1.y; qv[6] = a1.z; qv[7] = a1.w;
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qv[e] = qf[kQS ? 0 : h][c][e];
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc0 = fmaf(qv[2 * e], bf16lo(w[e]), acc0);
+            acc1 = fmaf(qv[2 * e + 1], bf16hi(w[e]), acc1);
+          }
+        }
+        float x = acc0 + acc1;
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        sc[p][h] = valid[p] ? x : -INFINITY;
+      }
+    }
+
+    // Online softmax: one (warp-uniform) max update per stage.
+    float pr[2][G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float mx = fmaxf(sc[0][h], sc[1][h]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      if (mx > m[h]) {
+        const float alpha = fast_exp2(m[h] - mx);  // exp2(-inf) = 0 on the first stage
+        m[h] = mx;
+        l[h] *= alpha;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[h][c][e] *= alpha;
+      }
+      const float mu = m[h] == -INFINITY ? 0.f : m[h];
+      pr[0][h] = fast_exp2(sc[0][h] - mu);
+      pr[1][h] = fast_exp2(sc[1][h] - mu);
+      l[h] += pr[0][h] + pr[1][h];
+    }
+
+    // acc += p * v
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const int tl = (p * NS + sub) * 4 + tg;
+      const uint4* vr = reinterpret_cast<const uint4*>(Vs + (size_t)tl * row_elems + g * D);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        uint4 u = vr[c * 8 + li];
+        if (!valid[p]) u = make_uint4(0, 0, 0, 0);  // stale smem may hold NaN patterns
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[h][c][2 * e] = fmaf(pr[p][h], bf16lo(w[e]), acc[h][c][2 * e]);
+            acc[h][c][2 * e + 1] = fmaf(pr[p][h], bf16hi(w[e]), acc[h][c][2 * e + 1]);
+          }
+      }
+    }
+
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (++s == kStages) {
+      s = 0;
+      ph ^= 1u;
+    }
+
+    if (!(md.flags & F_LAST)) continue;
+
+    // ---- end of this CTA's segment of sequence b: reduce over the 4 token groups
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
+      l[h] += __shfl_xor_sync(0xffffffffu, l[h], 16);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          acc[h][c][e] += __shfl_xor_sync(0xffffffffu, acc[h][c][e], 8);
+          acc[h][c][e] += __shfl_xor_sync(0xffffffffu, acc[h][c][e], 16);
+        }
+    }
+    bool writer = true;
+    if (NS > 1) {
+      // Several warps share kv head g.  Hand-off through shared memory with
+      // bounded mbarrier waits: warps sub > 0 publish (acc, m, l) and arrive
+      // on xfull[g]; warp sub 0 waits, combines by log-sum-exp and releases
+      // the buffer through xfree[g] before the next segment's hand-off.
+      writer = sub == 0;
+      if (!writer) {
+        if (seg > 0 && !mbar_wait(&xfree[g], (uint32_t)((seg - 1) & 1), a.status)) return;
+        float* mine = xw + (size_t)warp * G * (D + 2);
+        if (tg == 0) {
+#pragma unroll
+          for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) mine[h * (D + 2) + (c * 8 + li) * 8 + e] = acc[h][c][e];
+            if (li == 0) {
+              mine[h * (D + 2) + D] = m[h];
+              mine[h * (D + 2) + D + 1] = l[h];
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xfull[g]);
+      } else {
+        if (!mbar_wait(&xfull[g], (uint32_t)(seg & 1), a.status)) return;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float M = m[h];
+          for (int k = 1; k < NS; ++k)
+            M = fmaxf(M, xw[(size_t)(g + k * Hkv) * G * (D + 2) + h * (D + 2) + D]);
+          const float Mu = M == -INFINITY ? 0.f : M;
+          const float w0 = fast_exp2(m[h] - Mu);
+          float ls = w0 * l[h];
+#pragma unroll
+          for (int c = 0; c < NCH; ++c)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[h][c][e] *= w0;
+          for (int k = 1; k < NS; ++k) {
+            const float* o = xw + (size_t)(g + k * Hkv) * G * (D + 2) + h * (D + 2);
+            const float w = fast_exp2(o[D] - Mu);
+            ls += w * o[D + 1];
+#pragma unroll
+            for (int c = 0; c < NCH; ++c)
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc[h][c][e] += w * o[(c * 8 + li) * 8 + e];
+          }
+          m[h] = M;
+          l[h] = ls;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xfree[g]);
+      }
+    }
+    ++seg;
+    if (!writer || tg != 0) continue;
+    if (!(md.flags & (F_ENTERED | F_EXITS))) {
+      // whole sequence inside this CTA: normalise and write bf16
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float inv = 1.f / l[h];
+        uint16_t* orow = a.out + (int64_t)b * a.out_stride + (int64_t)(g * G + h) * D;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          uint4 u;
+          u.x = pack_bf16x2(acc[h][c][0] * inv, acc[h][c][1] * inv);
+          u.y = pack_bf16x2(acc[h][c][2] * inv, acc[h][c][3] * inv);
+          u.z = pack_bf16x2(acc[h][c][4] * inv, acc[h][c][5] * inv);
+          u.w = pack_bf16x2(acc[h][c][6] * inv, acc[h][c][7] * inv);
+          *reinterpret_cast<uint4*>(orow + (c * 8 + li) * 8) = u;
+        }
+      }
+    } else {
+      const int slot = (md.flags & F_ENTERED) ? 0 : 1;
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float* dst =
+            a.part + (((size_t)blockIdx.x * 2 + slot) * a.num_heads + g * G + h) * part_stride<D>();
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+          float4* d4 = reinterpret_cast<float4*>(dst + (c * 8 + li) * 8);
+          d4[0] = make_float4(acc[h][c][0], acc[h][c][1], acc[h][c][2], acc[h][c][3]);
+          d4[1] = make_float4(acc[h][c][4], acc[h][c][5], acc[h][c][6], acc[h][c][7]);
+        }
+        if (li == 0) {
+          dst[D] = m[h];
+          dst[D + 1] = l[h];
+        }
+      }
+    }
+  }
+}
+
+template <int D, int G>
+__global__ void __maxnreg__(168) decode_split_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t* ringK = smem;
+  uint8_t* ringV = smem + kStages * stage_half_bytes<D>();
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + 2 * kStages * stage_half_bytes<D>());
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + kStages);
+  uint64_t* empty = full + kStages;
+  uint64_t* xfull = empty + kStages;
+  uint64_t* xfree = xfull + kConsumerWarps;
+  float* xw = reinterpret_cast<float*>(xfree + kConsumerWarps);
+  float* qs = xw + (size_t)kConsumerWarps * G * (D + 2);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    const int ns = kConsumerWarps / a.num_kv_heads;
+    for (int i = 0; i < kConsumerWarps; ++i) {
+      mbar_init(&xfull[i], ns > 1 ? ns - 1 : 1);
+      mbar_init(&xfree[i], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if ((threadIdx.x >> 5) == kConsumerWarps)
+    decode_producer<D>(a, ringK, ringV, meta, full, empty);
+  else
+    decode_consumer<D, G>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
+}
+
+// Combines the partials of every sequence that crosses a CTA boundary.
+// Block j handles the sequence that leaves CTA j, if it entered no earlier
+// boundary; the sequence's partials are CTA j's "exits" slot and the
+// "entered" slots of the following CTAs it reaches.
+template <int D>
+__global__ void __launch_bounds__(256) decode_merge_kernel(const float* __restrict__ part,
+                                                           const int* __restrict__ split_seq,
+                                                           int ctas, int num_heads,
+                                                           uint16_t* __restrict__ out,
+                                                           int64_t out_stride) {
+  const int j = blockIdx.x;
+  const int b = split_seq[j];
+  if (b < 0 || (j > 0 && split_seq[j - 1] == b)) return;
+  int last = j + 1;
+  while (last < ctas - 1 && split_seq[last] == b) ++last;
+  for (int idx = threadIdx.x; idx < num_heads * D; idx += blockDim.x) {
+    const int h = idx / D, e = idx - h * D;
+    float M = -INFINITY;
+    for (int i = j; i <= last; ++i) {
+      const int slot = i == j ? 1 : 0;
+      M = fmaxf(M, part[(((size_t)i * 2 + slot) * num_heads + h) * part_stride<D>() + D]);
+    }
+    float num = 0.f, den = 0.f;
+    for (int i = j; i <= last; ++i) {
+      const int slot = i == j ? 1 : 0;
+      const float* p = part + (((size_t)i * 2 + slot) * num_heads + h) * part_stride<D>();
+      const float w = fast_exp2(p[D] - M);
+      num += w * p[e];
+      den += w * p[D + 1];
+    }
+    const __nv_bfloat16 r = __float2bfloat16_rn(num / den);
+    out[(int64_t)b * out_stride + (int64_t)h * D + e] = *reinterpret_cast<const uint16_t*>(&r);
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_decode_t(const DecodeArgs& a, int ctas, cudaStream_t stream) {
+  const size_t smem = decode_smem_bytes<D, G>();
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_split_kernel<D, G><<<ctas, kThreads, smem, stream>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  decode_merge_kernel<D><<<ctas, 256, 0, stream>>>(a.part, a.split_seq, ctas, a.num_heads, a.out,
+                                                   a.out_stride);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_supported(int num_heads, int num_kv_heads, int head_dim) {
+  if (num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads) return false;
+  if (num_kv_heads != 1 && num_kv_heads != 2 && num_kv_heads != 4 && num_kv_heads != 8)
+    return false;
+  const int G = num_heads / num_kv_heads;
+  if (head_dim == 128) return G == 1 || G == 2 || G == 4;
+  if (head_dim == 64) return G == 1 || G == 2 || G == 4 || G == 8;
+  return false;
+}
+
+DecodePlan plan_decode(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                       int num_sms) {
+  DecodePlan p{};
+  long long upper = (long long)num_seqs * (max_context_len > 0 ? max_context_len : 0);
+  long long ctas = (upper + 63) / 64;  // at least 64 tokens per CTA
+  if (ctas > num_sms) ctas = num_sms;
+  if (ctas < 1) ctas = 1;
+  p.ctas = (int)ctas;
+  p.part_bytes = (size_t)ctas * 2 * num_heads * (head_dim + 4) * sizeof(float);
+  p.split_bytes = (size_t)ctas * sizeof(int);
+  p.total_bytes = ((p.part_bytes + 255) / 256) * 256 + ((p.split_bytes + 255) / 256) * 256;
+  return p;
+}
+
+cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k_cache,
+                          const uint16_t* v_cache, int64_t num_blocks, int block_size,
+                          const int32_t* block_tables, int max_blocks, const int32_t* ctx,
+                          int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                          float softmax_scale, const DecodePlan& plan, void* workspace,
+                          uint16_t* out, int64_t out_stride, int* status, cudaStream_t stream) {
+  DecodeArgs a;
+  a.q = q;
+  a.q_stride = q_stride;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.num_blocks = num_blocks;
+  a.block_size = block_size;
+  a.block_tables = block_tables;
+  a.max_blocks = max_blocks;
+  a.ctx = ctx;
+  a.num_seqs = num_seqs;
+  a.num_heads = num_heads;
+  a.num_kv_heads = num_kv_heads;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.part = reinterpret_cast<float*>(workspace);
+  a.split_seq = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(workspace) +
+                                       ((plan.part_bytes + 255) / 256) * 256);
+  a.out = out;
+  a.out_stride = out_stride;
+  a.status = status;
+  const int G = num_heads / num_kv_heads;
+  if (head_dim == 128) {
+    switch (G) {
+      case 1: return launch_decode_t<128, 1>(a, plan.ctas, stream);
+      case 2: return launch_decode_t<128, 2>(a, plan.ctas, stream);
+      case 4: return launch_decode_t<128, 4>(a, plan.ctas, stream);
+    }
+  } else if (head_dim == 64) {
+    switch (G) {
+      case 1: return launch_decode_t<64, 1>(a, plan.ctas, stream);
+      case 2: return launch_decode_t<64, 2>(a, plan.ctas, stream);
+      case 4: return launch_decode_t<64, 4>(a, plan.ctas, stream);
+      case 8: return launch_decode_t<64, 8>(a, plan.ctas, stream);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace kvp

@@ -1,0 +1,86 @@
+// kv_store: slot-mapped scatter of a step's new K/V rows into the paged cache.
+//
+// Source: "nano-vLLM-1", ModelRunner "4. prefill 输入打包" / "5. deocde 输入打包"
+// (slot_mapping: linear slot block_id * block_size + offset of every new token;
+// -1 marks CUDA-graph padding) and "Nano vLLM 解读（5）：解析 ModelRunner" (the
+// [k/v, layer, block, offset, kv_head, head_dim] cache).
+//
+// One warp copies one (token, K-or-V) row of num_kv_heads * head_dim bf16
+// values.  With the 16-byte path every lane moves whole 16-byte vectors: the
+// row is read once (streaming, no L1 allocation) and written once.  HBM
+// traffic is the algorithmic minimum: 2 * N * row bytes read + the same written.
+#include "kvp_device.cuh"
+
+namespace kvp {
+namespace {
+
+constexpr int kStoreThreads = 256;
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+template <bool kVec16>
+__global__ void __launch_bounds__(kStoreThreads) kv_store_kernel(
+    const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int64_t k_stride,
+    int64_t v_stride, const int32_t* __restrict__ slots, int64_t n, uint16_t* __restrict__ k_cache,
+    uint16_t* __restrict__ v_cache, int64_t total_slots, int row_elems, int* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (kStoreThreads / 32);
+  for (int64_t r = (int64_t)blockIdx.x * (kStoreThreads / 32) + (threadIdx.x >> 5); r < 2 * n;
+       r += warps) {
+    const int64_t t = r >> 1;
+    const bool is_v = r & 1;
+    const int64_t s = slots[t];
+    if (s < 0) continue;  // padding slot: nothing to write
+    if (s >= total_slots) {
+      if (lane == 0) record_error(status, KVP_ERR_DEVICE_DATA);
+      continue;
+    }
+    const uint16_t* src = is_v ? v + t * v_stride : k + t * k_stride;
+    uint16_t* dst = (is_v ? v_cache : k_cache) + s * (int64_t)row_elems;
+    if constexpr (kVec16) {
+      const int nvec = row_elems >> 3;
+      const uint4* s4 = reinterpret_cast<const uint4*>(src);
+      uint4* d4 = reinterpret_cast<uint4*>(dst);
+      int i = lane;
+      for (; i + 96 < nvec; i += 128) {  // four vectors in flight per lane
+        uint4 a = ld_stream(s4 + i), b = ld_stream(s4 + i + 32), c = ld_stream(s4 + i + 64),
+              d = ld_stream(s4 + i + 96);
+        d4[i] = a;
+        d4[i + 32] = b;
+        d4[i + 64] = c;
+        d4[i + 96] = d;
+      }
+      for (; i < nvec; i += 32) d4[i] = ld_stream(s4 + i);
+    } else {
+      for (int i = lane; i < row_elems; i += 32) dst[i] = src[i];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_store(const uint16_t* k, const uint16_t* v, int64_t k_stride,
+                            int64_t v_stride, const int32_t* slots, int64_t n, uint16_t* k_cache,
+                            uint16_t* v_cache, int64_t total_slots, int row_elems, bool vec16,
+                            int num_sms, int* status, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  const int64_t rows_per_cta = kStoreThreads / 32;
+  int64_t grid = (2 * n + rows_per_cta - 1) / rows_per_cta;
+  const int64_t cap = (int64_t)num_sms * 16;
+  if (grid > cap) grid = cap;
+  if (vec16)
+    kv_store_kernel<true><<<(unsigned)grid, kStoreThreads, 0, stream>>>(
+        k, v, k_stride, v_stride, slots, n, k_cache, v_cache, total_slots, row_elems, status);
+  else
+    kv_store_kernel<false><<<(unsigned)grid, kStoreThreads, 0, stream>>>(
+        k, v, k_stride, v_stride, slots, n, k_cache, v_cache, total_slots, row_elems, status);
+  return cudaGetLastError();
+}
+
+}  // namespace kvp

@@ -1,0 +1,47 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units of libkvpaged.  Not installed; not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kvpaged.h"
+
+namespace kvp {
+
+// kv_store.cu
+cudaError_t launch_kv_store(const uint16_t* k, const uint16_t* v, int64_t k_stride,
+                            int64_t v_stride, const int32_t* slots, int64_t n, uint16_t* k_cache,
+                            uint16_t* v_cache, int64_t total_slots, int row_elems, bool vec16,
+                            int num_sms, int* status, cudaStream_t stream);
+
+// decode.cu
+struct DecodePlan {
+  int ctas;            // persistent CTAs of the split kernel (one per SM at most)
+  size_t part_bytes;   // partial results: ctas * 2 * Hq * (D + 4) floats
+  size_t split_bytes;  // one int per CTA
+  size_t total_bytes;  // workspace needed
+};
+DecodePlan plan_decode(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                       int num_sms);
+bool decode_supported(int num_heads, int num_kv_heads, int head_dim);
+cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k_cache,
+                          const uint16_t* v_cache, int64_t num_blocks, int block_size,
+                          const int32_t* block_tables, int max_blocks, const int32_t* ctx,
+                          int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                          float softmax_scale, const DecodePlan& plan, void* workspace,
+                          uint16_t* out, int64_t out_stride, int* status, cudaStream_t stream);
+
+// prefill.cu
+bool prefill_supported(int num_heads, int num_kv_heads, int head_dim, int block_size);
+int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const uint16_t* k,
+                   const uint16_t* v, int64_t kv_stride, int64_t total_k,
+                   const uint16_t* k_cache, const uint16_t* v_cache,
+                   int64_t num_blocks, int block_size, const int32_t* block_tables,
+                   int max_blocks, const int32_t* cu_q, const int32_t* cu_k, int max_seqlen_q,
+                   int max_seqlen_k, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                   float softmax_scale, uint16_t* out, int64_t out_stride, int num_sms,
+                   int* status, cudaStream_t stream, const char** why);
+
+}  // namespace kvp

@@ -1,0 +1,41 @@
+"""The C-ABI library builds (nvcc cross-compiles for sm_103a without a GPU),
+loads, and exports every function include/kvpaged.h declares.  No kernels run."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_125_gb300 as kvp
+from paged_kv_cache_125_gb300 import _build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kvpaged.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"^(?:const\s+)?\w[\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M))
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    return _build.build()
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    assert {"kv_store", "attn_prefill_varlen", "attn_decode_paged"} <= names
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_the_header(lib_path):
+    assert set(kvp.SIGNATURES) == declared_functions()
+    lib = kvp.library()
+    assert lib.kvp_version() >= 100
+    assert lib.kvp_last_error() == b""

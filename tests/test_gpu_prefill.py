@@ -1,0 +1,88 @@
+"""GPU parity: attn_prefill_varlen (tcgen05 path) against the CPU oracle, and the
+whole store -> prefill -> decode pipeline of the tiny configuration."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_125_gb300 as kvp
+from paged_kv_cache_125_gb300 import workloads as W
+
+from parity import assert_attn_close, assert_status_ok, run_gpu, run_oracle, u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    kvp.device_status()
+    yield
+    assert_status_ok()
+
+
+def _check(w, rows_for=None):
+    outs, kc, vc = run_gpu(w)
+    ref, kr, vr = run_oracle(w, rows_for=rows_for)
+    assert np.array_equal(u16(kc), kr) and np.array_equal(u16(vc), vr), "cache differs after kv_store"
+    res = []
+    for i, (o, r) in enumerate(zip(outs, ref)):
+        mask = None if rows_for is None or not w.steps[i].is_prefill else rows_for(i)
+        res.append(assert_attn_close(o, r, f"{w.name} step {i}", mask))
+    return res
+
+
+def test_config1_tiny_pipeline():
+    """Store the cached prefix, prefill 17 + 284 tokens (paged: the second prompt
+    has a cached block), then 4 decode steps; bs 16, d 64, Hq 2 / Hkv 1."""
+    _check(W.config1_tiny())
+
+
+def test_config3_full_size():
+    """8 prompts U[256, 2048], 0-2 cached blocks each, Qwen3-8B heads, bs 256."""
+    _check(W.config3_prefill())
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,lens,cached", [
+    (2, 2, 64, 16, [1, 2, 129, 300], [0, 0, 0, 0]),            # G=1, packed (no prefix)
+    (4, 2, 128, 16, [45, 200, 333], [1, 0, 4]),                  # G=2, paged, bs 16
+    (8, 2, 128, 32, [640, 70], [5, 2]),                          # G=4, bs 32
+    (16, 2, 64, 256, [1000, 257, 256], [1, 0, 0]),               # G=8, d 64
+    (32, 8, 128, 256, [2048, 1, 130], [7, 0, 0]),                # Qwen3-8B heads, long prefix
+    (16, 8, 128, 128, [777, 128, 129], [2, 0, 1]),               # bs 128
+    (8, 8, 128, 64, [300, 301, 302, 303, 304], [0, 1, 2, 3, 4]),
+    (4, 1, 64, 16, [17, 300], [0, 1]),
+    (16, 8, 128, 256, [100, 900, 2000, 37], [0, 0, 0, 0]),       # packed, several kv tiles
+])
+def test_prefill_shapes(hq, hkv, d, bs, lens, cached):
+    nb = sum(W.num_blocks_for(L, bs) for L in lens) + 5
+    w = W.prefill_workload(f"pf_{hq}_{hkv}_{d}_{bs}", lens, cached, hq, hkv, d, bs, nb)
+    _check(w)
+
+
+def test_prefill_fully_cached_prompt_has_no_rows():
+    """A block-aligned prompt whose every block hit the prefix cache has
+    q_len 0; the other sequences are unaffected."""
+    w = W.prefill_workload("fully_cached", [64, 100], [4, 1], 4, 2, 64, 16, 32)
+    m = w.steps[0].attn.meta
+    assert m.cu_seqlens_q.tolist()[:2] == [0, 0]
+    _check(w)
+
+
+def test_prefill_then_decode_matches_oracle_qwen3_shapes():
+    w = W.prefill_workload("pf_then_decode", [300, 513, 1200], [1, 2, 0], 16, 8, 128, 256, 32,
+                           extra_decode_steps=3)
+    _check(w)
+
+
+def test_prefill_out_of_range_block_is_flagged():
+    w = W.prefill_workload("bad", [100, 60], [1, 1], 4, 2, 128, 16, 32)
+    kc, vc = w.new_cache("cuda")
+    for st in w.setup + [w.steps[0].store]:
+        kvp.kv_store(st.k.cuda(), st.v.cuda(), st.slot_mapping.cuda(), kc, vc)
+    a = w.steps[0].attn
+    bt = a.meta.block_tables.clone()
+    bt[0, 2] = 9999
+    kvp.attn_prefill_varlen(a.q.cuda(), a.meta.cu_seqlens_q.cuda(), a.meta.cu_seqlens_k.cuda(),
+                            a.meta.max_seqlen_q, a.meta.max_seqlen_k, k_cache=kc, v_cache=vc,
+                            block_tables=bt.cuda())
+    assert kvp.device_status() == -6
