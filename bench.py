@@ -1,0 +1,494 @@
+#!/usr/bin/env python
+"""Benchmark of the paged KV-cache attention hot path on GB300.
+
+One step = one pass of the hot path over one batch of the decode workload
+(64 sequences, Qwen3-0.6B attention shape 16/8/128, context_lens uniform in
+[512, 4096], block_size 256, blocks shuffled over a 2048-block pool):
+kv_store of the step's 64 new K/V rows, then attn_decode_paged (split kernel +
+log-sum-exp merge).  The step is replayed from a CUDA graph (graph-safe
+decode, as the serving engine runs it) over 4 independent input sets in
+rotation, so no step finds its inputs in L2 (8.6 GB footprint vs 126 MB L2).
+
+value = algorithmic bytes of the step (K/V of every context token read once,
+q, out, new rows stored, block-table entries, context_lens) / step time, in
+GB/s.  The same line carries the prefill half of the metric (varlen prefill
+with prefix cache, 8 prompts, Qwen3-8B heads): causal FLOPs / time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own replica of
+the batch (the path shards by sequence with no exchange), time = max over
+ranks, value = total bytes / time ("weak" scaling).  --impl reference times
+the CPU oracle (fp64 C, all host cores) on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention HBM GB/s (% of peak); prefill attention TFLOP/s (% peak)"
+N_SETS = 4
+
+# DRAM bytes per launch from ncu (dram__bytes_read.sum + dram__bytes_write.sum)
+# for the dominant kernels, with the sha256 of the kernel source they were
+# measured on; a figure whose source has changed since is reported as null.
+TRAFFIC = {
+    "decode": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu", "sha256": None, "bytes": None},
+    "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu", "sha256": None, "bytes": None},
+}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--prefill-steps", type=int, default=None)
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-prefill", action="store_true")
+    return p.parse_args()
+
+
+def dist_info():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+def traffic_for(name):
+    t = TRAFFIC[name]
+    if t["bytes"] is None or t["sha256"] is None:
+        return None
+    src = open(os.path.join(ROOT, t["file"]), "rb").read()
+    return t["bytes"] if hashlib.sha256(src).hexdigest() == t["sha256"] else None
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def stop(self, windows=()):
+        """Summary of the samples taken inside the given (t0, t1) windows."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, ln in self.lines:
+            if windows and not any(t0 <= ts <= t1 for t0, t1 in windows):
+                continue
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- workloads
+
+def decode_bytes(w):
+    """Algorithmic bytes of one step: (store) read k, v rows + write them into
+    the cache; (decode) K and V of every context token once, q, out, the used
+    block-table entries and context_lens."""
+    a = w.steps[0].attn.meta
+    b = a.context_lens.numel()
+    row = w.num_kv_heads * w.head_dim * 2
+    ctx = a.context_lens.long()
+    store = 4 * b * row
+    kv = int(ctx.sum()) * row * 2
+    qo = 2 * b * w.num_heads * w.head_dim * 2
+    tables = int(((ctx + w.block_size - 1) // w.block_size).sum()) * 4 + b * 4
+    return store, kv + qo + tables
+
+
+def prefill_flops(w):
+    m = w.steps[0].attn.meta
+    q = (m.cu_seqlens_q[1:] - m.cu_seqlens_q[:-1]).long()
+    k = (m.cu_seqlens_k[1:] - m.cu_seqlens_k[:-1]).long()
+    c = k - q
+    visible = int((q * c + q * (q + 1) // 2).sum())
+    return 4 * w.head_dim * w.num_heads * visible
+
+
+class DeviceSet:
+    """One resident copy of a workload's step inputs and cache on the device."""
+
+    def __init__(self, w, device):
+        import torch
+        kc, vc = w.new_cache(device, poison=True)
+        w.place_history(kc, vc)
+        for st in w.setup:
+            self._store(st, kc, vc, device)
+        step = w.steps[0]
+        s, a = step.store, step.attn
+        self.k, self.v = s.k.to(device), s.v.to(device)
+        self.slots = s.slot_mapping.to(device)
+        self.q = a.q.to(device)
+        self.kc, self.vc = kc, vc
+        m = a.meta
+        if step.is_prefill:
+            self.cu_q, self.cu_k = m.cu_seqlens_q.to(device), m.cu_seqlens_k.to(device)
+            self.max_q, self.max_k = m.max_seqlen_q, m.max_seqlen_k
+            self.bt = None if m.block_tables is None else m.block_tables.to(device)
+            self.out = torch.empty_like(self.q)
+        else:
+            self.bt, self.ctx = m.block_tables.to(device), m.context_lens.to(device)
+            self.max_ctx = m.max_context_len
+            self.out = torch.empty_like(self.q)
+
+    @staticmethod
+    def _store(st, kc, vc, device):
+        import paged_kv_cache_125_gb300 as kvp
+        kvp.kv_store(st.k.to(device), st.v.to(device), st.slot_mapping.to(device), kc, vc)
+
+
+def store_call(kvp, s):
+    kvp.kv_store(s.k, s.v, s.slots, s.kc, s.vc)
+
+
+def decode_call(kvp, s, w, ws):
+    kvp.attn_decode_paged(s.q, s.kc, s.vc, s.bt, s.ctx, s.max_ctx, softmax_scale=w.scale,
+                          workspace=ws, out=s.out)
+
+
+def prefill_call(kvp, s, w):
+    kvp.attn_prefill_varlen(s.q, s.cu_q, s.cu_k, s.max_q, s.max_k, k=s.k, v=s.v, k_cache=s.kc,
+                            v_cache=s.vc, block_tables=s.bt, num_kv_heads=w.num_kv_heads,
+                            softmax_scale=w.scale, out=s.out)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def capture(fn, sets, stream):
+    """One CUDA graph per input set for the callable fn(set)."""
+    import torch
+    graphs = []
+    for s in sets:
+        fn(s)  # first use outside capture (library set-up)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn(s)
+        graphs.append(g)
+    torch.cuda.synchronize()
+    return graphs
+
+
+def timed_loop(store_graphs, attn_graphs, steps, warmup, world):
+    """One step = store graph + attention graph of input set i % n.  K steps
+    are timed between barrier + synchronize pairs; an event pair around every
+    attention graph (on the launching stream, outside the graphs) gives the
+    attention call's duration inside the timed region.
+    Returns (ms per step, mean ms of the attention call, wall window)."""
+    import torch
+    n = len(store_graphs)
+    for i in range(warmup):
+        store_graphs[i % n].replay()
+        attn_graphs[i % n].replay()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    start.record()
+    for i in range(steps):
+        store_graphs[i % n].replay()
+        evs[i][0].record()
+        attn_graphs[i % n].replay()
+        evs[i][1].record()
+    stop.record()
+    torch.cuda.synchronize()
+    w1 = time.perf_counter()
+    barrier(world)
+    ms_step = start.elapsed_time(stop) / steps
+    durs = [a.elapsed_time(b) for a, b in evs]
+    return ms_step, statistics.mean(durs), (w0, w1)
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_decode_rate(w, min_seconds=8.0):
+    """The oracle (fp64 C, all host cores) on the whole decode step (store +
+    decode of all 64 sequences), repeated until min_seconds have passed."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from parity import oracle_pool
+    kc, vc = oracle_pool(w)
+    st, a = w.steps[0].store, w.steps[0].attn
+    m = a.meta
+    q_cpu = a.q.cpu()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.kv_store(st.k.cpu(), st.v.cpu(), st.slot_mapping.cpu(), kc, vc)
+        oracle.decode(q_cpu, kc, vc, m.block_tables, m.context_lens, w.num_heads, w.num_kv_heads,
+                      w.scale)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds:
+            break
+    store, dec = decode_bytes(w)
+    return (store + dec) * reps / el / 1e9, el / reps, reps, oracle.num_threads()
+
+
+# ----------------------------------------------------------------------------- main arms
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on the host cores, on the same workload and
+    metric: each step is the full decode step (store + decode of all 64
+    sequences); at most --steps steps and about 60 s of timed work."""
+    if rank != 0:
+        return
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    from parity import oracle_pool
+    from paged_kv_cache_125_gb300 import workloads as W
+    w = W.config2_decode()
+    kc, vc = oracle_pool(w)
+    st, a = w.steps[0].store, w.steps[0].attn
+    m = a.meta
+
+    def step():
+        oracle.kv_store(st.k, st.v, st.slot_mapping, kc, vc)
+        oracle.decode(a.q, kc, vc, m.block_tables, m.context_lens, w.num_heads, w.num_kv_heads, w.scale)
+
+    for _ in range(min(args.warmup, 1)):
+        step()
+    done, t0 = 0, time.perf_counter()
+    while done < args.steps and (done == 0 or time.perf_counter() - t0 < 60.0):
+        step()
+        done += 1
+    el = time.perf_counter() - t0
+    store, dec = decode_bytes(w)
+    value = (store + dec) * done / el / 1e9
+    cores = oracle.num_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": done, "warmup": min(args.warmup, 1),
+            "ms_per_step": round(1000 * el / done, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.description, "parallelism": f"{cores} host threads"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": f"full decode step (store + decode of all 64 sequences) x {done}"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import paged_kv_cache_125_gb300 as kvp
+    from paged_kv_cache_125_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+
+    # ---------------- decode step (the headline)
+    w = W.config2_decode()
+    store_b, dec_b = decode_bytes(w)
+    step_bytes = store_b + dec_b
+    sets = [DeviceSet(w, dev) for _ in range(N_SETS)]
+    ws = torch.empty(kvp.attn_decode_workspace_size(64, w.num_heads, w.head_dim,
+                                                    w.steps[0].attn.meta.max_context_len,
+                                                    w.block_size), dtype=torch.uint8, device=dev)
+    store_graphs = capture(lambda s: store_call(kvp, s), sets, stream)
+    dec_graphs = capture(lambda s: decode_call(kvp, s, w, ws), sets, stream)
+    assert kvp.device_status() == 0
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    smi_id = f"GPU-{uuid}" if uuid is not None else str(local)
+    sampler = ClockSampler(smi_id)
+    sampler.start()
+    time.sleep(0.3)
+    ms_step, ms_decode, win = timed_loop(store_graphs, dec_graphs, args.steps, args.warmup, world)
+    windows = [win]
+    assert kvp.device_status() == 0, "device status after the timed decode loop"
+    ms_step = max_over_ranks(ms_step, world)
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    dec_achieved = dec_b / (ms_decode * 1e-3) / 1e9
+    tr = traffic_for("decode")
+    roofline = {"kernel": "attn_decode_paged (split + merge)", "bound": "hbm",
+                "achieved": round(dec_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(dec_achieved / peaks["hbm_gbs"], 4), "traffic": tr,
+                "algorithmic_bytes": dec_b, "peak_source": peaks["source"], "ms_per_launch": round(ms_decode, 5)}
+
+    # ---------------- e2e through the API with host buffers (pinned), per step
+    s0 = sets[0]
+    host_in = [t.cpu().pin_memory() for t in (s0.q, s0.k, s0.v, s0.slots, s0.bt, s0.ctx)]
+    host_out = torch.empty(s0.out.shape, dtype=s0.out.dtype, pin_memory=True)
+    dev_in = [s0.q, s0.k, s0.v, s0.slots, s0.bt, s0.ctx]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        for hsrc, dst in zip(host_in, dev_in):
+            dst.copy_(hsrc, non_blocking=True)
+        store_graphs[0].replay()
+        dec_graphs[0].replay()
+        host_out.copy_(s0.out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(5):
+        e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    e2e = {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+           "how": "pinned host inputs copied in, graph replay, output copied out, stream sync each step"}
+    del store_graphs, dec_graphs
+
+    # ---------------- prefill half of the metric
+    prefill = None
+    if not args.no_prefill:
+        wp = W.config3_prefill()
+        flops = prefill_flops(wp)
+        psets = [DeviceSet(wp, dev) for _ in range(N_SETS)]
+        pstore = capture(lambda s: store_call(kvp, s), psets, stream)
+        pattn = capture(lambda s: prefill_call(kvp, s, wp), psets, stream)
+        psteps = args.prefill_steps or max(50, args.steps // 4)
+        ms_pstep, ms_prefill, pwin = timed_loop(pstore, pattn, psteps, args.warmup, world)
+        windows.append(pwin)
+        assert kvp.device_status() == 0, "device status after the timed prefill loop"
+        ms_pstep = max_over_ranks(ms_pstep, world)
+        tflops_kernel = flops / (ms_prefill * 1e-3) / 1e12
+        prefill = {"workload": wp.description, "value": round(flops * world / (ms_pstep * 1e-3) / 1e12, 2),
+                   "unit": "TFLOP/s", "ms_per_step": round(ms_pstep, 4), "steps": psteps,
+                   "step": "kv_store of the uncached suffix + attn_prefill_varlen (paged, prefix cache)",
+                   "roofline": {"kernel": "attn_prefill_varlen", "bound": "tensor",
+                                "achieved": round(tflops_kernel, 1), "peak": peaks["bf16_tflops"],
+                                "unit": "TFLOP/s", "frac": round(tflops_kernel / peaks["bf16_tflops"], 4),
+                                "traffic": traffic_for("prefill"), "algorithmic_flops": flops,
+                                "peak_source": peaks["source"] + " bf16 burst",
+                                "ms_per_launch": round(ms_prefill, 5)}}
+        del pstore, pattn, psets
+
+    time.sleep(0.1)
+    clocks = sampler.stop(windows)
+
+    # ---------------- CPU baseline (the oracle on the host cores)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, sec, reps, cores = oracle_decode_rate(w, min_seconds=8.0)
+        cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"full decode step (store + decode, 64 sequences) x {reps}, {sec:.2f} s each"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic",
+                "config": {"workload": w.description, "step": "kv_store (64 new rows) + attn_decode_paged",
+                           "global_batch": 64 * world, "parallelism": f"replicas x{world}",
+                           "l2": f"{N_SETS} input sets in rotation ({N_SETS * 2.15:.1f} GB) > 126 MB L2",
+                           "graph": "each step is one CUDA graph replay"},
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": 3 * args.steps, "clocks": clocks, "prefill": prefill}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
