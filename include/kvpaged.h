@@ -182,6 +182,43 @@ int attn_decode_paged(const kvp_bf16 *q, int64_t q_stride_tok, const kvp_bf16 *k
                       void *workspace, size_t workspace_bytes, kvp_bf16 *out,
                       int64_t out_stride_tok, kvp_stream_t stream);
 
+/*
+ * attn_decode_paged_noalloc - attn_decode_paged for callers that cannot
+ * allocate device memory.
+ *
+ * The pages have no counterpart to this call; it exists for integration.
+ * Some callers have no way to obtain device memory on the call path: a
+ * plugin inside a host runtime that owns every allocation and hands out no
+ * allocator, a real-time serving loop that forbids cudaMalloc after start-up
+ * (it can block and synchronize the device), or code that must not add an
+ * allocation failure mode.  This entry point needs no workspace argument:
+ * the split partials go into a scratch array compiled into the library
+ * (a file-scope device variable of 8 MiB).  It calls no cudaMalloc, cudaFree
+ * or other allocating routine.
+ *
+ * Arguments, results and errors are those of attn_decode_paged without
+ * `workspace` / `workspace_bytes`.  In addition:
+ * - a shape whose scratch need (attn_decode_workspace_size) exceeds 8 MiB is
+ *   rejected with KVP_ERR_WORKSPACE and a message naming both sizes, before
+ *   any other check; on a 152-SM GB300 every shape attn_decode_paged
+ *   supports fits;
+ * - every GPU that loads the library reserves the 8 MiB until the process
+ *   exits;
+ * - the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) and caches it; make that first call before any
+ *   stream capture on that device;
+ * - all calls share the one array and each call overwrites it (nothing in
+ *   it needs to start at zero): calls that can overlap on the GPU (different
+ *   streams, or different host threads without ordering) race and must not be
+ *   issued; calls in order on one stream are safe.
+ */
+int attn_decode_paged_noalloc(const kvp_bf16 *q, int64_t q_stride_tok, const kvp_bf16 *k_cache,
+                              const kvp_bf16 *v_cache, int64_t num_blocks, int block_size,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, int num_seqs, int max_context_len,
+                              int num_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                              kvp_bf16 *out, int64_t out_stride_tok, kvp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

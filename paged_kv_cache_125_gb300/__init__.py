@@ -19,6 +19,7 @@ import os
 import threading
 
 __all__ = ["kv_store", "attn_prefill_varlen", "attn_decode_paged", "attn_decode_workspace_size",
+           "attn_decode_paged_noalloc",
            "device_status", "library", "library_path", "KvpError"]
 
 _LIB_LOCK = threading.Lock()
@@ -41,6 +42,8 @@ SIGNATURES = {
     "attn_decode_workspace_size": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "attn_decode_paged": (_I32, [_P, _I64, _P, _P, _I64, _I32, _P, _I32, _P, _I32, _I32, _I32, _I32,
                                  _I32, _F32, _P, _SZ, _P, _I64, _P]),
+    "attn_decode_paged_noalloc": (_I32, [_P, _I64, _P, _P, _I64, _I32, _P, _I32, _P, _I32, _I32, _I32,
+                                         _I32, _I32, _F32, _P, _I64, _P]),
 }
 
 
@@ -173,6 +176,34 @@ def attn_decode_paged(q, k_cache, v_cache, block_tables, context_lens, max_conte
         block_tables.shape[1], _ptr(context_lens), b, int(max_context_len), hq, hkv, d, scale,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), os_,
         _stream(k_cache)))
+    return out
+
+
+def attn_decode_paged_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
+                              softmax_scale: float | None = None, out=None):
+    """attn_decode_paged without a workspace: the library's built-in scratch
+    is used (see include/kvpaged.h for who needs this and its limits)."""
+    import torch
+    nb, bs, hkv, d = _cache_dims(k_cache, v_cache)
+    dev = k_cache.device
+    _require(q, "q", torch.bfloat16, 3, dev)
+    b, hq = q.shape[0], q.shape[1]
+    qs = _rows(q, "q", hq, d)
+    _require(block_tables, "block_tables", torch.int32, 2, dev)
+    _require(context_lens, "context_lens", torch.int32, 1, dev)
+    if block_tables.shape[0] != b or context_lens.shape[0] != b:
+        raise ValueError("block_tables / context_lens must have one row per sequence")
+    if not block_tables.is_contiguous() or not context_lens.is_contiguous():
+        raise ValueError("block_tables / context_lens must be contiguous")
+    if out is None:
+        out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=dev)
+    _require(out, "out", torch.bfloat16, 3, dev)
+    os_ = _rows(out, "out", hq, d)
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    _check(library().attn_decode_paged_noalloc(
+        _ptr(q), qs, _ptr(k_cache), _ptr(v_cache), nb, bs, _ptr(block_tables),
+        block_tables.shape[1], _ptr(context_lens), b, int(max_context_len), hq, hkv, d, scale,
+        _ptr(out), os_, _stream(k_cache)))
     return out
 
 

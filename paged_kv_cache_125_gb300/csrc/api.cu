@@ -62,6 +62,18 @@ bool valid_block_size_pow2(int bs) {
 
 }  // namespace
 
+namespace kvp {
+
+int set_last_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+}  // namespace kvp
+
 extern "C" {
 
 const char* kvp_last_error(void) { return g_last_error; }

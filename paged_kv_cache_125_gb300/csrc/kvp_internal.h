@@ -10,6 +10,9 @@
 
 namespace kvp {
 
+// api.cu: records the calling thread's message for kvp_last_error(); returns code.
+int set_last_error(int code, const char* fmt, ...);
+
 // kv_store.cu
 cudaError_t launch_kv_store(const uint16_t* k, const uint16_t* v, int64_t k_stride,
                             int64_t v_stride, const int32_t* slots, int64_t n, uint16_t* k_cache,
