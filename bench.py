@@ -59,6 +59,9 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--only", choices=["decode", "prefill"], default=None,
+                   help="run one half only (profiling); the JSON line then carries that half")
+    p.add_argument("--sets", type=int, default=N_SETS, help="input sets in rotation")
     return p.parse_args()
 
 
@@ -225,14 +228,23 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x, world):
+def max_over_ranks(x, world, device="cuda"):
+    """Largest value of x over all ranks (per-step time: the slowest rank
+    defines the job's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate(step_units, ms_per_rank, world, device="cuda"):
+    """Whole-job throughput of `world` replicas that each process step_units
+    per step: total units / max-over-ranks step time (units per second)."""
+    ms = max_over_ranks(ms_per_rank, world, device)
+    return step_units * world / (ms * 1e-3), ms
 
 
 def capture(fn, sets, stream):
@@ -351,47 +363,30 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def run_ours(args, rank, world, local):
+def measure_decode(args, kvp, W, dev, stream, world, peaks):
     import torch
-    import paged_kv_cache_125_gb300 as kvp
-    from paged_kv_cache_125_gb300 import workloads as W
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    peaks = load_peaks()
-    stream = torch.cuda.Stream(dev)
-    torch.cuda.set_stream(stream)
-
-    # ---------------- decode step (the headline)
     w = W.config2_decode()
     store_b, dec_b = decode_bytes(w)
     step_bytes = store_b + dec_b
-    sets = [DeviceSet(w, dev) for _ in range(N_SETS)]
+    sets = [DeviceSet(w, dev) for _ in range(args.sets)]
     ws = torch.empty(kvp.attn_decode_workspace_size(64, w.num_heads, w.head_dim,
                                                     w.steps[0].attn.meta.max_context_len,
                                                     w.block_size), dtype=torch.uint8, device=dev)
     store_graphs = capture(lambda s: store_call(kvp, s), sets, stream)
     dec_graphs = capture(lambda s: decode_call(kvp, s, w, ws), sets, stream)
     assert kvp.device_status() == 0
-    props = torch.cuda.get_device_properties(dev)
-    uuid = getattr(props, "uuid", None)
-    smi_id = f"GPU-{uuid}" if uuid is not None else str(local)
-    sampler = ClockSampler(smi_id)
-    sampler.start()
-    time.sleep(0.3)
     ms_step, ms_decode, win = timed_loop(store_graphs, dec_graphs, args.steps, args.warmup, world)
-    windows = [win]
     assert kvp.device_status() == 0, "device status after the timed decode loop"
-    ms_step = max_over_ranks(ms_step, world)
-    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    bytes_per_s, ms_step = aggregate(step_bytes, ms_step, world)
     dec_achieved = dec_b / (ms_decode * 1e-3) / 1e9
-    tr = traffic_for("decode")
-    roofline = {"kernel": "attn_decode_paged (split + merge)", "bound": "hbm",
-                "achieved": round(dec_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(dec_achieved / peaks["hbm_gbs"], 4), "traffic": tr,
-                "algorithmic_bytes": dec_b, "peak_source": peaks["source"], "ms_per_launch": round(ms_decode, 5)}
+    res = {"w": w, "window": win, "ms_step": ms_step, "value": bytes_per_s / 1e9,
+           "roofline": {"kernel": "attn_decode_paged (split + merge)", "bound": "hbm",
+                        "achieved": round(dec_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(dec_achieved / peaks["hbm_gbs"], 4), "traffic": traffic_for("decode"),
+                        "algorithmic_bytes": dec_b, "peak_source": peaks["source"],
+                        "ms_per_launch": round(ms_decode, 5)}}
 
-    # ---------------- e2e through the API with host buffers (pinned), per step
+    # end to end through the API with host buffers (pinned), per step
     s0 = sets[0]
     host_in = [t.cpu().pin_memory() for t in (s0.q, s0.k, s0.v, s0.slots, s0.bt, s0.ctx)]
     host_out = torch.empty(s0.out.shape, dtype=s0.out.dtype, pin_memory=True)
@@ -414,59 +409,89 @@ def run_ours(args, rank, world, local):
     for _ in range(args.e2e_steps):
         e2e_step()
     e2e_ms = (time.perf_counter() - t0) * 1e3 / args.e2e_steps
-    e2e_ms = max_over_ranks(e2e_ms, world)
-    e2e = {"value": round(step_bytes * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-           "how": "pinned host inputs copied in, graph replay, output copied out, stream sync each step"}
-    del store_graphs, dec_graphs
+    e2e_bps, e2e_ms = aggregate(step_bytes, e2e_ms, world)
+    res["e2e"] = {"value": round(e2e_bps / 1e9, 2), "unit": "GB/s",
+                  "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+                  "how": "pinned host inputs copied in, graph replay, output copied out, stream sync each step"}
+    res["footprint_gb"] = sum(2 * s.kc.numel() * 2 for s in sets) / 1e9
+    del store_graphs, dec_graphs, sets
+    return res
 
-    # ---------------- prefill half of the metric
-    prefill = None
-    if not args.no_prefill:
-        wp = W.config3_prefill()
-        flops = prefill_flops(wp)
-        psets = [DeviceSet(wp, dev) for _ in range(N_SETS)]
-        pstore = capture(lambda s: store_call(kvp, s), psets, stream)
-        pattn = capture(lambda s: prefill_call(kvp, s, wp), psets, stream)
-        psteps = args.prefill_steps or max(50, args.steps // 4)
-        ms_pstep, ms_prefill, pwin = timed_loop(pstore, pattn, psteps, args.warmup, world)
-        windows.append(pwin)
-        assert kvp.device_status() == 0, "device status after the timed prefill loop"
-        ms_pstep = max_over_ranks(ms_pstep, world)
-        tflops_kernel = flops / (ms_prefill * 1e-3) / 1e12
-        prefill = {"workload": wp.description, "value": round(flops * world / (ms_pstep * 1e-3) / 1e12, 2),
-                   "unit": "TFLOP/s", "ms_per_step": round(ms_pstep, 4), "steps": psteps,
-                   "step": "kv_store of the uncached suffix + attn_prefill_varlen (paged, prefix cache)",
-                   "roofline": {"kernel": "attn_prefill_varlen", "bound": "tensor",
-                                "achieved": round(tflops_kernel, 1), "peak": peaks["bf16_tflops"],
-                                "unit": "TFLOP/s", "frac": round(tflops_kernel / peaks["bf16_tflops"], 4),
-                                "traffic": traffic_for("prefill"), "algorithmic_flops": flops,
-                                "peak_source": peaks["source"] + " bf16 burst",
-                                "ms_per_launch": round(ms_prefill, 5)}}
-        del pstore, pattn, psets
 
+def measure_prefill(args, kvp, W, dev, stream, world, peaks):
+    wp = W.config3_prefill()
+    flops = prefill_flops(wp)
+    psets = [DeviceSet(wp, dev) for _ in range(args.sets)]
+    pstore = capture(lambda s: store_call(kvp, s), psets, stream)
+    pattn = capture(lambda s: prefill_call(kvp, s, wp), psets, stream)
+    psteps = args.prefill_steps or max(50, args.steps // 4)
+    ms_pstep, ms_prefill, pwin = timed_loop(pstore, pattn, psteps, args.warmup, world)
+    assert kvp.device_status() == 0, "device status after the timed prefill loop"
+    flops_per_s, ms_pstep = aggregate(flops, ms_pstep, world)
+    tflops_kernel = flops / (ms_prefill * 1e-3) / 1e12
+    del pstore, pattn, psets
+    return {"window": pwin,
+            "line": {"workload": wp.description, "value": round(flops_per_s / 1e12, 2),
+                     "unit": "TFLOP/s", "ms_per_step": round(ms_pstep, 4), "steps": psteps,
+                     "step": "kv_store of the uncached suffix + attn_prefill_varlen (paged, prefix cache)",
+                     "roofline": {"kernel": "attn_prefill_varlen", "bound": "tensor",
+                                  "achieved": round(tflops_kernel, 1), "peak": peaks["bf16_tflops"],
+                                  "unit": "TFLOP/s", "frac": round(tflops_kernel / peaks["bf16_tflops"], 4),
+                                  "traffic": traffic_for("prefill"), "algorithmic_flops": flops,
+                                  "peak_source": peaks["source"] + " bf16 burst",
+                                  "ms_per_launch": round(ms_prefill, 5)}}}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import paged_kv_cache_125_gb300 as kvp
+    from paged_kv_cache_125_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    sampler = ClockSampler(f"GPU-{uuid}" if uuid is not None else str(local))
+    sampler.start()
+    time.sleep(0.3)
+    windows = []
+    dec = pre = None
+    if args.only != "prefill":
+        dec = measure_decode(args, kvp, W, dev, stream, world, peaks)
+        windows.append(dec["window"])
+    if args.only != "decode" and not args.no_prefill:
+        pre = measure_prefill(args, kvp, W, dev, stream, world, peaks)
+        windows.append(pre["window"])
     time.sleep(0.1)
     clocks = sampler.stop(windows)
 
-    # ---------------- CPU baseline (the oracle on the host cores)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, sec, reps, cores = oracle_decode_rate(w, min_seconds=8.0)
+    if dec is not None and rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, sec, reps, cores = oracle_decode_rate(dec["w"], min_seconds=8.0)
         cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"full decode step (store + decode, 64 sequences) x {reps}, {sec:.2f} s each"}
-
-    if rank == 0:
-        line = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-                "data": "synthetic",
-                "config": {"workload": w.description, "step": "kv_store (64 new rows) + attn_decode_paged",
-                           "global_batch": 64 * world, "parallelism": f"replicas x{world}",
-                           "l2": f"{N_SETS} input sets in rotation ({N_SETS * 2.15:.1f} GB) > 126 MB L2",
-                           "graph": "each step is one CUDA graph replay"},
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": 3 * args.steps, "clocks": clocks, "prefill": prefill}
-        print(json.dumps(line), flush=True)
+    if rank != 0:
+        return
+    if dec is None:  # profiling run of the prefill half only
+        print(json.dumps({"metric": METRIC, "only": "prefill", "clocks": clocks, "prefill": pre["line"]}),
+              flush=True)
+        return
+    w = dec["w"]
+    line = {"metric": METRIC, "value": round(dec["value"], 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dec["ms_step"], 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.description, "step": "kv_store (64 new rows) + attn_decode_paged",
+                       "global_batch": 64 * world, "parallelism": f"replicas x{world}",
+                       "l2": f"{args.sets} input sets in rotation ({dec['footprint_gb']:.1f} GB of pools) vs 126 MB L2",
+                       "graph": "each step is two CUDA graph replays (store, attention)"},
+            "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
+            "gpu_launches": 3 * args.steps, "clocks": clocks,
+            "prefill": None if pre is None else pre["line"]}
+    print(json.dumps(line), flush=True)
 
 
 def main():

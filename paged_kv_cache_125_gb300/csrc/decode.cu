@@ -513,6 +513,8 @@ __global__ void __maxnreg__(168) decode_split_kernel(const DecodeArgs a) {
   float* qs = xw + (size_t)kConsumerWarps * G * (D + 2);
 
   if (threadIdx.x == 0) {
+    // The merge kernel may be scheduled now; it waits for this grid to finish.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
@@ -532,38 +534,37 @@ __global__ void __maxnreg__(168) decode_split_kernel(const DecodeArgs a) {
 }
 
 // Combines the partials of every sequence that crosses a CTA boundary.
-// Block j handles the sequence that leaves CTA j, if it entered no earlier
-// boundary; the sequence's partials are CTA j's "exits" slot and the
-// "entered" slots of the following CTAs it reaches.
+// Block (j, h) handles query head h of the sequence that leaves CTA j, if that
+// sequence did not also enter CTA j; its partials are CTA j's "exits" slot
+// and the "entered" slots of the following CTAs it reaches.  One thread per
+// element of head_dim.  Launched as a programmatic dependent of the split
+// kernel: it may start while the split kernel drains and waits for the split
+// grid's completion (and memory flush) before reading anything.
 template <int D>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const float* __restrict__ part,
-                                                           const int* __restrict__ split_seq,
-                                                           int ctas, int num_heads,
-                                                           uint16_t* __restrict__ out,
-                                                           int64_t out_stride) {
-  const int j = blockIdx.x;
+__global__ void __launch_bounds__(D) decode_merge_kernel(const float* __restrict__ part,
+                                                         const int* __restrict__ split_seq,
+                                                         int ctas, int num_heads,
+                                                         uint16_t* __restrict__ out,
+                                                         int64_t out_stride) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int j = blockIdx.x, h = blockIdx.y, e = threadIdx.x;
   const int b = split_seq[j];
   if (b < 0 || (j > 0 && split_seq[j - 1] == b)) return;
   int last = j + 1;
   while (last < ctas - 1 && split_seq[last] == b) ++last;
-  for (int idx = threadIdx.x; idx < num_heads * D; idx += blockDim.x) {
-    const int h = idx / D, e = idx - h * D;
-    float M = -INFINITY;
-    for (int i = j; i <= last; ++i) {
-      const int slot = i == j ? 1 : 0;
-      M = fmaxf(M, part[(((size_t)i * 2 + slot) * num_heads + h) * part_stride<D>() + D]);
-    }
-    float num = 0.f, den = 0.f;
-    for (int i = j; i <= last; ++i) {
-      const int slot = i == j ? 1 : 0;
-      const float* p = part + (((size_t)i * 2 + slot) * num_heads + h) * part_stride<D>();
-      const float w = fast_exp2(p[D] - M);
-      num += w * p[e];
-      den += w * p[D + 1];
-    }
-    const __nv_bfloat16 r = __float2bfloat16_rn(num / den);
-    out[(int64_t)b * out_stride + (int64_t)h * D + e] = *reinterpret_cast<const uint16_t*>(&r);
+  constexpr int S = part_stride<D>();
+  float M = -INFINITY;
+  for (int i = j; i <= last; ++i)
+    M = fmaxf(M, part[(((size_t)i * 2 + (i == j ? 1 : 0)) * num_heads + h) * S + D]);
+  float num = 0.f, den = 0.f;
+  for (int i = j; i <= last; ++i) {
+    const float* p = part + (((size_t)i * 2 + (i == j ? 1 : 0)) * num_heads + h) * S;
+    const float w = fast_exp2(p[D] - M);
+    num += w * p[e];
+    den += w * p[D + 1];
   }
+  const __nv_bfloat16 r = __float2bfloat16_rn(num / den);
+  out[(int64_t)b * out_stride + (int64_t)h * D + e] = *reinterpret_cast<const uint16_t*>(&r);
 }
 
 template <int D, int G>
@@ -575,9 +576,18 @@ cudaError_t launch_decode_t(const DecodeArgs& a, int ctas, cudaStream_t stream) 
   decode_split_kernel<D, G><<<ctas, kThreads, smem, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_merge_kernel<D><<<ctas, 256, 0, stream>>>(a.part, a.split_seq, ctas, a.num_heads, a.out,
-                                                   a.out_stride);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas, a.num_heads);
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<D>, (const float*)a.part,
+                            (const int*)a.split_seq, ctas, a.num_heads, a.out, a.out_stride);
 }
 
 }  // namespace

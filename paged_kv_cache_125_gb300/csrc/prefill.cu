@@ -40,9 +40,10 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per kv tile
-constexpr int kThreadsPF = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kSoftmaxWarps = 8;  // two threads per query row, 64 columns each
+constexpr int kThreadsPF = (kSoftmaxWarps + 2) * 32;
+constexpr int kProducerWarp = kSoftmaxWarps;
+constexpr int kMmaWarp = kSoftmaxWarps + 1;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct PrefillArgs {
@@ -77,10 +78,14 @@ struct Layout {
   static constexpr uint32_t kK = kQ + 2 * kQBytes;     // 2 slots
   static constexpr uint32_t kV = kK + 2 * kKVBytes;    // 2 slots
   static constexpr uint32_t kP = kV + 2 * kKVBytes;    // 1 buffer
-  static constexpr uint32_t kBar = kP + kPBytes;
-  static constexpr uint32_t kNumBars = 18;
+  static constexpr uint32_t kX = kP + kPBytes;      // row-half exchange [2][2][128] fp32
+  static constexpr uint32_t kBar = kX + 2 * 2 * kBM * 4;
+  static constexpr uint32_t kNumBars = 22;
   static constexpr uint32_t kTotal = kBar + kNumBars * 8 + 16;
-  static constexpr uint32_t kAlloc = kTotal + 1024;    // slack for 1 KiB alignment
+  // The dynamic shared memory base is 1 KiB aligned on this architecture (the
+  // kernel checks it and reports KVP_ERR_DEVICE_DATA otherwise); keep a small
+  // slack only.
+  static constexpr uint32_t kAlloc = kTotal + 128;
 };
 
 // Barrier indices.
@@ -96,6 +101,7 @@ enum : int {
   B_ODONE = 15,
   B_OFREE = 16,
   B_DRAIN = 17,
+  B_XCH = 18,    // [4]: the two warps of one lane quarter exchange row halves
 };
 
 struct Item {
@@ -364,98 +370,139 @@ drain:
 template <int D>
 __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, uint32_t tbase) {
   using Lay = Layout<D>;
-  const int r = threadIdx.x;  // 0..127: query row == TMEM lane
-  const int warp = r >> 5, lane = r & 31;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  constexpr int kHalfCols = kBN / 2;  // S / P columns per thread
+  constexpr int kHalfD = D / 2;       // O columns per thread
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter, column half
+  const int r = quarter * 32 + lane;                // query row == TMEM lane
+  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
   uint8_t* sP = smem + Lay::kP;
+  float* xbuf = reinterpret_cast<float*>(smem + Lay::kX);  // [parity][half][row]
+  uint64_t* xbar = &bars[B_XCH + quarter];
+  uint32_t xcnt = 0;  // exchanges so far (identical in both warps of a quarter)
+
+  // The two threads of a row swap one value through shared memory; bounded
+  // wait on the quarter's barrier; double-buffered by exchange parity.
+  auto exchange = [&](float mine, float& theirs) -> bool {
+    const int par = xcnt & 1;
+    xbuf[(par * 2 + half) * kBM + r] = mine;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(xbar);
+    if (!mbar_wait(xbar, (uint32_t)par, a.status)) return false;
+    theirs = xbuf[(par * 2 + (half ^ 1)) * kBM + r];
+    ++xcnt;
+    return true;
+  };
+
   TileIter t;
   iter_begin(a, t);
+  const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
   while (t.valid) {
     const Item it = t.it;
     const int tok = r / a.group, h = r - tok * a.group;
     const bool row_valid = tok < it.rows_tok;
     const int pos = it.cached + it.q0 + (row_valid ? tok : it.rows_tok - 1);
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;  // l: this thread's half of the row sum
     for (int j = 0; j < it.n_tiles; ++j) {
       const uint32_t jt = t.jt;
       const int st = jt & 1;
       if (!mbar_wait(&bars[B_SFULL + st], (jt >> 1) & 1, a.status)) return;
       tc_fence_after();
-      float s[kBN];
+      float s[kHalfCols];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = 0; c < kHalfCols / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tbase + lane_base + st * kBN + c * 32, v);
+        tmem_ld32(tbase + lane_base + st * kBN + half * kHalfCols + c * 32, v);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
       }
-      const int lim = pos - j * kBN;  // columns <= lim are visible
-      if (lim < kBN - 1) {
+      const int lim = pos - j * kBN - half * kHalfCols;  // my columns <= lim are visible
+      if (lim < kHalfCols - 1) {
 #pragma unroll
-        for (int i = 0; i < kBN; ++i)
+        for (int i = 0; i < kHalfCols; ++i)
           if (i > lim) s[i] = -INFINITY;
       }
-      float mx = -INFINITY;
+      float mx4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int i = 0; i < kBN; ++i) mx = fmaxf(mx, s[i]);
+      for (int i = 4; i < kHalfCols; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+      float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      float other;
+      if (!exchange(mx, other)) return;
+      mx = fmaxf(mx, other);
       const float mxs = mx * a.scale_log2;
+      // The reference max m only moves when the tile's max exceeds it by more
+      // than 2^8 (or on the first tile): O and l then get rescaled by alpha.
+      float alpha = 1.f;
+      bool rescale = false;
       if (j == 0) {
         m = mxs;  // key 0 is visible to every row: finite
-      } else {
+      } else if (mxs > m + kRescaleThreshold) {
+        alpha = fast_exp2(m - mxs);
+        m = mxs;
+        rescale = true;
+      }
+      // P = exp2(s * scale_log2 - m) as bf16 pairs, computed while the previous
+      // tile's PV still runs on the tensor core.
+      const float2 negm = make_float2(-m, -m);
+      uint32_t pk[kHalfCols / 2];
+      float2 sum2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int i = 0; i < kHalfCols / 2; ++i) {
+        const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scale2, negm);
+        const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+        sum2 = __fadd2_rn(sum2, p);
+        pk[i] = pack_bf16x2(p.x, p.y);
+      }
+      if (j > 0) {
         // PV of the previous tile has finished: O is stable and P is free.
         if (!mbar_wait(&bars[B_ODONE], (jt - 1) & 1, a.status)) return;
         tc_fence_after();
-        if (mxs > m + kRescaleThreshold) {
-          const float alpha = fast_exp2(m - mxs);
+        if (rescale) {
           l *= alpha;
-          m = mxs;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
+          for (int c = 0; c < kHalfD / 32; ++c) {
             uint32_t v[32];
-            const uint32_t addr = tbase + lane_base + 2 * kBN + c * 32;
+            const uint32_t addr = tbase + lane_base + 2 * kBN + half * kHalfD + c * 32;
             tmem_ld32(addr, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            for (int i = 0; i < 32; i += 2) {
+              const float2 o = __fmul2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                          make_float2(alpha, alpha));
+              v[i] = __float_as_uint(o.x);
+              v[i + 1] = __float_as_uint(o.y);
+            }
             tmem_st32(addr, v);
           }
           tmem_st_wait();
         }
       }
-      // P = exp2(s * scale_log2 - m) as bf16, written in the swizzled K-major layout.
-      float rowsum = 0.f;
+      l += sum2.x + sum2.y;
+      // P into shared memory, 128-byte swizzled K-major (the PV MMA's A
+      // operand): this thread's 64 keys are exactly 64-key panel `half`.
 #pragma unroll
-      for (int c = 0; c < kBN / 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(fmaf(s[c * 8 + 2 * e], a.scale_log2, -m));
-          const float p1 = fast_exp2(fmaf(s[c * 8 + 2 * e + 1], a.scale_log2, -m));
-          w[e] = pack_bf16x2(p0, p1);
-          rowsum += bf16lo(w[e]) + bf16hi(w[e]);
-        }
-        const int panel = c >> 3, cc = c & 7;
-        *reinterpret_cast<uint4*>(sP + panel * Lay::kPanelBytes + r * 128 + ((cc ^ (r & 7)) << 4)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
-      l += rowsum;
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(sP + half * Lay::kPanelBytes + r * 128 + ((c ^ (r & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_PFULL]);
       iter_next(a, t);
     }
-    // Epilogue: O / l -> bf16 -> out.
+    // Epilogue: O / l -> bf16 -> out; each thread stores its half of the row.
     if (!mbar_wait(&bars[B_ODONE], (t.jt - 1) & 1, a.status)) return;
     tc_fence_after();
-    const float inv = 1.f / l;
+    float l_other;
+    if (!exchange(l, l_other)) return;
+    const float inv = 1.f / (l + l_other);
     uint16_t* orow = a.out + (int64_t)(it.q_row0 + tok) * a.out_stride +
-                     (int64_t)(it.g * a.group + h) * D;
+                     (int64_t)(it.g * a.group + h) * D + half * kHalfD;
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int c = 0; c < kHalfD / 32; ++c) {
       uint32_t v[32];
-      tmem_ld32(tbase + lane_base + 2 * kBN + c * 32, v);
+      tmem_ld32(tbase + lane_base + 2 * kBN + half * kHalfD + c * 32, v);
       tmem_ld_wait();
       if (row_valid) {
 #pragma unroll
@@ -480,9 +527,12 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const PrefillArgs a) {
   using Lay = Layout<D>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // the 128-byte swizzle needs a 1 KiB aligned base
+    if (threadIdx.x == 0) record_error(a.status, KVP_ERR_DEVICE_DATA);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Lay::kNumBars);
   const int warp = threadIdx.x >> 5;
@@ -497,10 +547,11 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
       mbar_init(&bars[B_VEMPTY + i], 1);
       mbar_init(&bars[B_SFULL + i], 1);
     }
-    mbar_init(&bars[B_PFULL], 4);
+    mbar_init(&bars[B_PFULL], kSoftmaxWarps);
     mbar_init(&bars[B_ODONE], 1);
-    mbar_init(&bars[B_OFREE], 4);
+    mbar_init(&bars[B_OFREE], kSoftmaxWarps);
     mbar_init(&bars[B_DRAIN], 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars[B_XCH + i], 2);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
