@@ -8,27 +8,37 @@
 // positions start at num_cached_tokens); attention is softmax(QK^T/sqrt(d))V
 // with the causal mask of "【nano-vllm 学习】04 …", "KV-Cache … 是什么？".
 //
-// Work unit ("item"): one sequence b, one kv head g, and a tile of 128 query
-// rows = 128/G tokens x the G query heads that share kv head g, so every K/V
-// tile in shared memory serves all G heads in one MMA.  Query row (token t,
-// head h) sits at absolute position c_b + q0 + t and sees keys 0 .. that
-// position.  An item walks kv tiles of 128 keys up to its last visible key.
+// Work unit ("item"): one sequence b, one kv head g and two query tiles A and
+// B of 128 rows each.  A tile row is (token, head): 128/G consecutive tokens
+// x the G query heads that share kv head g, so one MMA serves the whole GQA
+// group; tile B holds the 128/G tokens that follow tile A's.  Query row
+// (token t, head h) sits at absolute position c_b + t and sees keys 0 .. that
+// position.  An item walks kv tiles of 128 keys up to the last key its last
+// row sees; each K/V tile in shared memory feeds both query tiles, which
+// halves the K/V bytes moved per FLOP compared with one tile.
 //
-// Persistent CTAs (one per SM), 6 warps:
-//   warp 4  TMA producer: Q tile (2 slots), K tiles (2 slots), V tiles
+// Persistent CTAs (one per SM), 10 warps:
+//   warp 8  TMA producer: the Q pair (one slot), K tiles (2 slots), V tiles
 //           (2 slots).  In paged mode a kv tile is loaded as block-sized
 //           sub-boxes addressed through the block table (gather folded into
-//           the loads).
-//   warp 5  MMA issuer + tensor-memory owner.  S_j = Q K_j^T into one of two
-//           128-column TMEM buffers (issued two tiles ahead of the PV
-//           stream), O += P_j V_j into a third TMEM region.
-//   warps 0-3 softmax / correction / epilogue: thread r owns query row r
-//           (TMEM lane r).  Reads S with tcgen05.ld, masks only where the
-//           tile crosses the diagonal, keeps a running max per row and
-//           rescales O only when the max grows by more than 2^8 (exact: O and
-//           the row sum share the stale reference), writes P as bf16 into
-//           shared memory in the 128-byte-swizzled K-major layout the MMA
-//           reads, and at the end of an item normalises O and stores bf16.
+//           the loads); sub-boxes past the sequence's last key are skipped.
+//   warp 9  MMA issuer + tensor-memory owner.  TMEM columns: S_A | S_B | O_A |
+//           O_B (128 each).  Issue order per kv tile j:
+//             PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+//           so each softmax warpgroup computes on one tile while the tensor
+//           core works on the other tile (ping-pong).
+//   warps 0-3 / 4-7  softmax for tile A / B: thread r owns row r (TMEM lane
+//           r).  Reads S with tcgen05.ld, masks only where a tile crosses the
+//           diagonal, keeps a running max per row and rescales O only when
+//           the max grows by more than 2^8 (exact: O and the row sum share the
+//           stale reference), writes P as bf16 into shared memory in the
+//           128-byte-swizzled K-major layout the MMA reads, and at the end of
+//           an item normalises O and stores bf16.
+// Synchronisation facts the design relies on: a tcgen05.commit arrives only
+// when every earlier MMA of the issuing thread has completed, so the commit
+// after S_X(j) also says PV_X(j-1) is done (O_X may be rescaled).  The single
+// P buffer alternates between the tiles in MMA order; before writing P each
+// warpgroup waits for the PV that read P last.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -40,10 +50,18 @@ namespace {
 
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per kv tile
-constexpr int kSoftmaxWarps = 8;  // two threads per query row, 64 columns each
-constexpr int kThreadsPF = (kSoftmaxWarps + 2) * 32;
-constexpr int kProducerWarp = kSoftmaxWarps;
-constexpr int kMmaWarp = kSoftmaxWarps + 1;
+// Three warpgroups: softmax A (warps 0-3), softmax B (4-7), and a control
+// group (warp 8 TMA producer, warp 9 MMA issuer, warps 10-11 idle).  The
+// launch gives every thread 168 registers (384 x 168 = 64512); the control
+// group hands registers back with setmaxnreg and the softmax groups take them:
+// 128 x (200 + 200 + 104) = 64512, the launch's total.
+constexpr int kThreadsPF = 384;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kSoftmaxRegs = 200;
+constexpr int kControlRegs = 104;
+static_assert(128 * (2 * kSoftmaxRegs + kControlRegs) <= kThreadsPF * 168,
+              "register split exceeds the launch's allotment");
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 struct PrefillArgs {
@@ -57,10 +75,10 @@ struct PrefillArgs {
   int num_seqs;
   int num_heads;
   int num_kv_heads;
-  int group;        // G
-  int tok_per_tile; // 128 / G
-  int sub_rows;     // rows per TMA box of a kv tile (paged: min(bs, 128))
-  int max_tiles;    // ceil(max_seqlen_q / tok_per_tile)
+  int group;         // G
+  int tok_per_tile;  // 128 / G
+  int sub_rows;      // rows per TMA box of a kv tile (paged: min(bs, 128))
+  int max_pairs;     // ceil(max_seqlen_q / (2 * tok_per_tile))
   float scale_log2;
   uint16_t* out;
   int64_t out_stride;
@@ -71,43 +89,41 @@ template <int D>
 struct Layout {
   static constexpr uint32_t kPanels = D / 64;
   static constexpr uint32_t kPanelBytes = 128 * 128;  // 128 rows x 128 bytes
-  static constexpr uint32_t kQBytes = kBM * D * 2;
+  static constexpr uint32_t kQBytes = kBM * D * 2;    // one query tile
   static constexpr uint32_t kKVBytes = kBN * D * 2;
   static constexpr uint32_t kPBytes = kBM * kBN * 2;
-  static constexpr uint32_t kQ = 0;                    // 2 slots
-  static constexpr uint32_t kK = kQ + 2 * kQBytes;     // 2 slots
-  static constexpr uint32_t kV = kK + 2 * kKVBytes;    // 2 slots
-  static constexpr uint32_t kP = kV + 2 * kKVBytes;    // 1 buffer
-  static constexpr uint32_t kX = kP + kPBytes;      // row-half exchange [2][2][128] fp32
-  static constexpr uint32_t kBar = kX + 2 * 2 * kBM * 4;
-  static constexpr uint32_t kNumBars = 22;
+  static constexpr uint32_t kQ = 0;                  // tiles A, B
+  static constexpr uint32_t kK = kQ + 2 * kQBytes;   // 2 slots
+  static constexpr uint32_t kV = kK + 2 * kKVBytes;  // 2 slots
+  static constexpr uint32_t kP = kV + 2 * kKVBytes;  // 1 buffer
+  static constexpr uint32_t kBar = kP + kPBytes;
+  static constexpr uint32_t kNumBars = 21;
   static constexpr uint32_t kTotal = kBar + kNumBars * 8 + 16;
   // The dynamic shared memory base is 1 KiB aligned on this architecture (the
-  // kernel checks it and reports KVP_ERR_DEVICE_DATA otherwise); keep a small
-  // slack only.
+  // kernel checks it and reports KVP_ERR_DEVICE_DATA otherwise).
   static constexpr uint32_t kAlloc = kTotal + 128;
 };
 
 // Barrier indices.
 enum : int {
-  B_QFULL = 0,   // [2]
-  B_QEMPTY = 2,  // [2]
-  B_KFULL = 4,   // [2]
-  B_KEMPTY = 6,  // [2]
-  B_VFULL = 8,   // [2]
-  B_VEMPTY = 10, // [2]
-  B_SFULL = 12,  // [2]
-  B_PFULL = 14,
-  B_ODONE = 15,
-  B_OFREE = 16,
-  B_DRAIN = 17,
-  B_XCH = 18,    // [4]: the two warps of one lane quarter exchange row halves
+  B_QFULL = 0,
+  B_QEMPTY = 1,
+  B_KFULL = 2,   // [2]
+  B_KEMPTY = 4,  // [2]
+  B_VFULL = 6,   // [2]
+  B_VEMPTY = 8,  // [2]
+  B_SFULL = 10,  // [2]: tile A, tile B
+  B_PFULL = 12,  // [2]
+  B_PVDONE = 14, // [2]
+  B_OFREE = 16,  // [2]
+  B_DRAIN = 18,
 };
 
 struct Item {
-  int b, g, q0, rows_tok, q_len, cached, k_len, kv_end, n_tiles;
-  int q_row0;   // packed row of the item's first query token
-  int k_row0;   // packed row of the sequence's first key (packed mode)
+  int b, g, q0, q_len, cached, k_len, n_tiles;
+  int rows_a, rows_b;  // valid tokens in tile A / B (rows_b may be 0)
+  int q_row0;          // packed row of tile A's first token
+  int k_row0;          // packed row of the sequence's first key (packed mode)
 };
 
 __device__ __forceinline__ bool decode_item(const PrefillArgs& a, int L, Item& it) {
@@ -124,17 +140,30 @@ __device__ __forceinline__ bool decode_item(const PrefillArgs& a, int L, Item& i
     if (it.q_len > 0 && r == 0 && it.g == 0) record_error(a.status, KVP_ERR_DEVICE_DATA);
     return false;
   }
-  const int ntiles = (it.q_len + a.tok_per_tile - 1) / a.tok_per_tile;
-  if (r >= ntiles) return false;
-  const int t = ntiles - 1 - r;  // heaviest tiles (largest t) come first
-  it.q0 = t * a.tok_per_tile;
-  it.rows_tok = min(a.tok_per_tile, it.q_len - it.q0);
+  const int span = 2 * a.tok_per_tile;
+  const int npairs = (it.q_len + span - 1) / span;
+  if (r >= npairs) return false;
+  const int t = npairs - 1 - r;  // heaviest pairs (largest t) come first
+  it.q0 = t * span;
+  it.rows_a = min(a.tok_per_tile, it.q_len - it.q0);
+  it.rows_b = max(0, min(a.tok_per_tile, it.q_len - it.q0 - a.tok_per_tile));
   it.cached = it.k_len - it.q_len;
-  it.kv_end = it.cached + it.q0 + it.rows_tok;  // keys visible to the last row
-  it.n_tiles = (it.kv_end + kBN - 1) / kBN;
+  const int kv_end = it.cached + it.q0 + it.rows_a + it.rows_b;  // keys the last row sees
+  it.n_tiles = (kv_end + kBN - 1) / kBN;
   it.q_row0 = cq0 + it.q0;
   it.k_row0 = ck0;
   return true;
+}
+
+__device__ __forceinline__ int total_items(const PrefillArgs& a) {
+  return a.max_pairs * a.num_seqs * a.num_kv_heads;
+}
+
+// Next item of this CTA at or after index L (items are dealt round-robin).
+__device__ __forceinline__ bool next_item(const PrefillArgs& a, int& L, Item& it) {
+  for (; L < total_items(a); L += gridDim.x)
+    if (decode_item(a, L, it)) return true;
+  return false;
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -155,43 +184,34 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
     prefetch_tensormap(tmK);
     prefetch_tensormap(tmV);
   }
-  const int total_items = a.max_tiles * a.num_seqs * a.num_kv_heads;
   int item_idx = 0;
   uint32_t jt = 0;
-  for (int L = blockIdx.x; L < total_items; L += gridDim.x) {
-    Item it;
-    if (!decode_item(a, L, it)) continue;
-    // Q tile: 128/G tokens x G heads x D, one box per 64-column panel.
-    {
-      const int slot = item_idx & 1;
-      const uint32_t par = (item_idx >> 1) & 1;
-      if (!mbar_wait(&bars[B_QEMPTY + slot], par ^ 1u, a.status)) return;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[B_QFULL + slot], Lay::kQBytes);
-        uint8_t* dst = smem + Lay::kQ + slot * Lay::kQBytes;
+  Item it;
+  for (int L = blockIdx.x; next_item(a, L, it); L += gridDim.x, ++item_idx) {
+    // Q pair: both tiles in one slot (tile B past the sequence is harmless
+    // data: its rows are never stored).
+    if (!mbar_wait(&bars[B_QEMPTY], (item_idx & 1) ^ 1u, a.status)) return;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars[B_QFULL], 2 * Lay::kQBytes);
+      for (int x = 0; x < 2; ++x)
         for (int p = 0; p < (int)Lay::kPanels; ++p)
-          tma_load_3d(dst + p * Lay::kPanelBytes, tmQ, p * 64, it.g * a.group, it.q_row0,
-                      &bars[B_QFULL + slot]);
-      }
+          tma_load_3d(smem + Lay::kQ + x * Lay::kQBytes + p * Lay::kPanelBytes, tmQ, p * 64,
+                      it.g * a.group, it.q_row0 + x * a.tok_per_tile, &bars[B_QFULL]);
     }
-    // Block ids of this item, 32 logical blocks per warp-wide window.
-    int win_base = -1, win_val = -1;
+    int win_base = -1, win_val = -1;  // 32 block-table entries per warp-wide window
     for (int j = 0; j < it.n_tiles; ++j, ++jt) {
       const int st = jt & 1;
       const uint32_t par = (jt >> 1) & 1;
-      // Rows of this tile that exist (keys < k_len); sub-boxes past them are not loaded.
       const int key0 = j * kBN;
       int nsub, rows_per_box;
       if (a.paged) {
         rows_per_box = a.sub_rows;
-        const int valid = min(kBN, it.k_len - key0);
-        nsub = (valid + rows_per_box - 1) / rows_per_box;
+        nsub = (min(kBN, it.k_len - key0) + rows_per_box - 1) / rows_per_box;
       } else {
         rows_per_box = kBN;
         nsub = 1;
       }
       const uint32_t bytes = (uint32_t)(nsub * rows_per_box * D * 2);
-      // physical row of every sub-box (paged: through the block table)
       int rowi[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) rowi[i] = 0;
@@ -230,105 +250,77 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
         }
       }
     }
-    ++item_idx;
   }
 }
 
 // ------------------------------------------------------------------ MMA issuer
 
-// Walks the (item, kv tile) sequence of this CTA.
-struct TileIter {
-  int L;        // current item index (global)
-  int j;        // tile within item
-  int item_idx; // items of this CTA so far
-  uint32_t jt;  // global tile counter
-  Item it;
-  bool valid;
-};
-
-__device__ __forceinline__ void iter_begin(const PrefillArgs& a, TileIter& t) {
-  const int total_items = a.max_tiles * a.num_seqs * a.num_kv_heads;
-  t.item_idx = 0;
-  t.jt = 0;
-  t.j = 0;
-  t.valid = false;
-  for (t.L = blockIdx.x; t.L < total_items; t.L += gridDim.x)
-    if (decode_item(a, t.L, t.it)) {
-      t.valid = true;
-      return;
-    }
-}
-
-__device__ __forceinline__ void iter_next(const PrefillArgs& a, TileIter& t) {
-  ++t.jt;
-  if (++t.j < t.it.n_tiles) return;
-  t.j = 0;
-  ++t.item_idx;
-  const int total_items = a.max_tiles * a.num_seqs * a.num_kv_heads;
-  t.valid = false;
-  for (t.L += gridDim.x; t.L < total_items; t.L += gridDim.x)
-    if (decode_item(a, t.L, t.it)) {
-      t.valid = true;
-      return;
-    }
+template <int D>
+__device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint32_t qa, uint32_t ka) {
+  using Lay = Layout<D>;
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (kk >> 2) * Lay::kPanelBytes + (kk & 3) * 32;
+    umma_f16_ss(d_tmem, smem_desc(qa + off, 16, 1024, 2), smem_desc(ka + off, 16, 1024, 2), idesc,
+                kk > 0);
+  }
 }
 
 template <int D>
-__device__ bool issue_s(const PrefillArgs& a, const TileIter& s, uint8_t* smem, uint64_t* bars,
-                        uint32_t tbase) {
+__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t pa, uint32_t va, bool acc) {
   using Lay = Layout<D>;
-  const int lane = threadIdx.x & 31;
-  const int qslot = s.item_idx & 1;
-  if (s.j == 0 && !mbar_wait(&bars[B_QFULL + qslot], (s.item_idx >> 1) & 1, a.status)) return false;
-  const int st = s.jt & 1;
-  if (!mbar_wait(&bars[B_KFULL + st], (s.jt >> 1) & 1, a.status)) return false;
-  tc_fence_after();
-  if (lane == 0) {
-    const uint32_t qa = smem_u32(smem + Lay::kQ + qslot * Lay::kQBytes);
-    const uint32_t ka = smem_u32(smem + Lay::kK + st * Lay::kKVBytes);
-    constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, 0, 0);
+  constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, 0, 1);
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t off = (kk >> 2) * Lay::kPanelBytes + (kk & 3) * 32;
-      umma_f16_ss(tbase + st * kBN, smem_desc(qa + off, 16, 1024, 2),
-                  smem_desc(ka + off, 16, 1024, 2), idesc, kk > 0);
-    }
-    umma_commit(&bars[B_SFULL + st]);
-    umma_commit(&bars[B_KEMPTY + st]);
-    if (s.j == s.it.n_tiles - 1) umma_commit(&bars[B_QEMPTY + qslot]);
+  for (int kk = 0; kk < kBN / 16; ++kk) {
+    const uint64_t ad = smem_desc(pa + (kk >> 2) * Lay::kPanelBytes + (kk & 3) * 32, 16, 1024, 2);
+    const uint64_t bd = smem_desc(va + kk * 16 * 128, Lay::kPanelBytes, 1024, 2);
+    umma_f16_ss(d_tmem, ad, bd, idesc, (acc || kk > 0) ? 1u : 0u);
   }
-  __syncwarp();
-  return true;
 }
 
 template <int D>
 __device__ void mma_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, uint32_t tbase) {
   using Lay = Layout<D>;
   const int lane = threadIdx.x & 31;
-  TileIter pv, sx;
-  iter_begin(a, pv);
-  iter_begin(a, sx);
-  // S for the first two tiles
-  for (int i = 0; i < 2 && sx.valid; ++i) {
-    if (!issue_s<D>(a, sx, smem, bars, tbase)) goto drain;
-    iter_next(a, sx);
-  }
-  while (pv.valid) {
-    {
-      const uint32_t jt = pv.jt;
+  const uint32_t qa[2] = {smem_u32(smem + Lay::kQ), smem_u32(smem + Lay::kQ + Lay::kQBytes)};
+  const uint32_t pa = smem_u32(smem + Lay::kP);
+  uint32_t ns[2] = {0, 0};    // S issued per tile
+  uint32_t np[2] = {0, 0};    // P consumed (PV issued) per tile
+  uint32_t nitems[2] = {0, 0};  // items per tile (A: all, B: those with rows)
+  int item_idx = 0;
+  uint32_t jt = 0;
+  Item it;
+  for (int L = blockIdx.x; next_item(a, L, it); L += gridDim.x, ++item_idx) {
+    const bool has_b = it.rows_b > 0;
+    const int ntile = has_b ? 2 : 1;
+    if (!mbar_wait(&bars[B_QFULL], item_idx & 1, a.status)) goto drain;
+    // S for kv tile 0
+    if (!mbar_wait(&bars[B_KFULL + (jt & 1)], (jt >> 1) & 1, a.status)) goto drain;
+    tc_fence_after();
+    if (lane == 0) {
+      const uint32_t ka = smem_u32(smem + Lay::kK + (jt & 1) * Lay::kKVBytes);
+      for (int x = 0; x < ntile; ++x) {
+        mma_qk<D>(tbase + x * kBN, qa[x], ka);
+        umma_commit(&bars[B_SFULL + x]);
+      }
+      umma_commit(&bars[B_KEMPTY + (jt & 1)]);
+      if (it.n_tiles == 1) umma_commit(&bars[B_QEMPTY]);
+    }
+    __syncwarp();
+    for (int x = 0; x < ntile; ++x) ++ns[x];
+    for (int j = 0; j < it.n_tiles; ++j, ++jt) {
       const int st = jt & 1;
-      if (!mbar_wait(&bars[B_PFULL], jt & 1, a.status)) goto drain;
-      if (pv.j == 0 && pv.item_idx > 0 &&
-          !mbar_wait(&bars[B_OFREE], (pv.item_idx - 1) & 1, a.status))
-        goto drain;
+      const bool more = j + 1 < it.n_tiles;
+      const uint32_t jn = jt + 1;
       if (!mbar_wait(&bars[B_VFULL + st], (jt >> 1) & 1, a.status)) goto drain;
       uint8_t* vs = smem + Lay::kV + st * Lay::kKVBytes;
       // Rows past the sequence's last key may hold stale or poisoned data;
       // P is 0 there, but 0 * NaN is NaN inside the MMA: zero them.
-      const int valid_rows = pv.it.k_len - pv.j * kBN;
+      const int valid_rows = it.k_len - j * kBN;
       if (valid_rows < kBN) {
         const int r0 = valid_rows < 0 ? 0 : valid_rows;
-        const int n16 = (kBN - r0) * 8;  // 16-byte chunks per panel
+        const int n16 = (kBN - r0) * 8;
         for (int p = 0; p < (int)Lay::kPanels; ++p)
           for (int i = lane; i < n16; i += 32)
             *reinterpret_cast<uint4*>(vs + p * Lay::kPanelBytes + r0 * 128 + i * 16) =
@@ -336,27 +328,36 @@ __device__ void mma_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, ui
         fence_proxy_async_smem();
         __syncwarp();
       }
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t pa = smem_u32(smem + Lay::kP);
-        const uint32_t va = smem_u32(vs);
-        constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, 0, 1);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t ad = smem_desc(pa + (kk >> 2) * Lay::kPanelBytes + (kk & 3) * 32, 16, 1024, 2);
-          const uint64_t bd = smem_desc(va + kk * 16 * 128, Lay::kPanelBytes, 1024, 2);
-          umma_f16_ss(tbase + 2 * kBN, ad, bd, idesc, (pv.j > 0 || kk > 0) ? 1u : 0u);
+      for (int x = 0; x < ntile; ++x) {
+        if (!mbar_wait(&bars[B_PFULL + x], np[x] & 1, a.status)) goto drain;
+        if (j == 0 && nitems[x] > 0 && !mbar_wait(&bars[B_OFREE + x], (nitems[x] - 1) & 1, a.status))
+          goto drain;
+        tc_fence_after();
+        if (lane == 0) {
+          mma_pv<D>(tbase + 2 * kBN + x * kBN, pa, smem_u32(vs), j > 0);
+          umma_commit(&bars[B_PVDONE + x]);
         }
+        __syncwarp();
+        if (more) {
+          if (!mbar_wait(&bars[B_KFULL + (jn & 1)], (jn >> 1) & 1, a.status)) goto drain;
+          tc_fence_after();
+          if (lane == 0) {
+            mma_qk<D>(tbase + x * kBN, qa[x], smem_u32(smem + Lay::kK + (jn & 1) * Lay::kKVBytes));
+            umma_commit(&bars[B_SFULL + x]);
+          }
+          __syncwarp();
+        }
+        ++np[x];
+        if (more) ++ns[x];
+      }
+      if (lane == 0) {
         umma_commit(&bars[B_VEMPTY + st]);
-        umma_commit(&bars[B_ODONE]);
+        if (more) umma_commit(&bars[B_KEMPTY + (jn & 1)]);
+        if (j + 2 == it.n_tiles) umma_commit(&bars[B_QEMPTY]);
       }
       __syncwarp();
     }
-    if (sx.valid) {
-      if (!issue_s<D>(a, sx, smem, bars, tbase)) goto drain;
-      iter_next(a, sx);
-    }
-    iter_next(a, pv);
+    for (int x = 0; x < ntile; ++x) ++nitems[x];
   }
 drain:
   // Every MMA this thread issued has completed before the CTA tears down.
@@ -370,69 +371,59 @@ drain:
 template <int D>
 __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, uint32_t tbase) {
   using Lay = Layout<D>;
-  constexpr int kHalfCols = kBN / 2;  // S / P columns per thread
-  constexpr int kHalfD = D / 2;       // O columns per thread
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter, column half
-  const int r = quarter * 32 + lane;                // query row == TMEM lane
-  const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+  const int x = warp >> 2;               // query tile: 0 = A, 1 = B
+  const int r = (warp & 3) * 32 + lane;  // row == TMEM lane
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t s_col = tbase + lane_base + x * kBN;
+  const uint32_t o_col = tbase + lane_base + 2 * kBN + x * kBN;
   uint8_t* sP = smem + Lay::kP;
-  float* xbuf = reinterpret_cast<float*>(smem + Lay::kX);  // [parity][half][row]
-  uint64_t* xbar = &bars[B_XCH + quarter];
-  uint32_t xcnt = 0;  // exchanges so far (identical in both warps of a quarter)
-
-  // The two threads of a row swap one value through shared memory; bounded
-  // wait on the quarter's barrier; double-buffered by exchange parity.
-  auto exchange = [&](float mine, float& theirs) -> bool {
-    const int par = xcnt & 1;
-    xbuf[(par * 2 + half) * kBM + r] = mine;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(xbar);
-    if (!mbar_wait(xbar, (uint32_t)par, a.status)) return false;
-    theirs = xbuf[(par * 2 + (half ^ 1)) * kBM + r];
-    ++xcnt;
-    return true;
-  };
-
-  TileIter t;
-  iter_begin(a, t);
   const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
-  while (t.valid) {
-    const Item it = t.it;
+  uint32_t ns = 0;                 // S tiles consumed by this tile's warpgroup
+  uint32_t npv[2] = {0, 0};        // PVs of tiles A / B that this thread has seen issued
+  bool prev_has_b = false, first = true;
+  Item it;
+  for (int L = blockIdx.x; next_item(a, L, it); L += gridDim.x) {
+    const bool has_b = it.rows_b > 0;
+    const int rows = x == 0 ? it.rows_a : it.rows_b;
+    if (x == 1 && !has_b) {
+      npv[0] += it.n_tiles;
+      prev_has_b = false;
+      first = false;
+      continue;
+    }
     const int tok = r / a.group, h = r - tok * a.group;
-    const bool row_valid = tok < it.rows_tok;
-    const int pos = it.cached + it.q0 + (row_valid ? tok : it.rows_tok - 1);
-    float m = -INFINITY, l = 0.f;  // l: this thread's half of the row sum
+    const bool row_valid = tok < rows;
+    const int tok0 = it.q0 + x * a.tok_per_tile;  // first token of this tile
+    const int pos = it.cached + tok0 + (row_valid ? tok : rows - 1);
+    float m = -INFINITY, l = 0.f;
     for (int j = 0; j < it.n_tiles; ++j) {
-      const uint32_t jt = t.jt;
-      const int st = jt & 1;
-      if (!mbar_wait(&bars[B_SFULL + st], (jt >> 1) & 1, a.status)) return;
+      if (!mbar_wait(&bars[B_SFULL + x], ns & 1, a.status)) return;
+      ++ns;
       tc_fence_after();
-      float s[kHalfCols];
+      float s[kBN];
 #pragma unroll
-      for (int c = 0; c < kHalfCols / 32; ++c) {
+      for (int c = 0; c < kBN / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tbase + lane_base + st * kBN + half * kHalfCols + c * 32, v);
+        tmem_ld32(s_col + c * 32, v);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
       }
-      const int lim = pos - j * kBN - half * kHalfCols;  // my columns <= lim are visible
-      if (lim < kHalfCols - 1) {
+      const int lim = pos - j * kBN;  // columns <= lim are visible
+      if (lim < kBN - 1) {
 #pragma unroll
-        for (int i = 0; i < kHalfCols; ++i)
+        for (int i = 0; i < kBN; ++i)
           if (i > lim) s[i] = -INFINITY;
       }
       float mx4[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-      for (int i = 4; i < kHalfCols; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
-      float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      float other;
-      if (!exchange(mx, other)) return;
-      mx = fmaxf(mx, other);
-      const float mxs = mx * a.scale_log2;
+      for (int i = 4; i < kBN; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], s[i]);
+      const float mxs = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * a.scale_log2;
       // The reference max m only moves when the tile's max exceeds it by more
       // than 2^8 (or on the first tile): O and l then get rescaled by alpha.
+      // The S commit of this tile implies the previous PV of this tile is
+      // complete, so O may be read and written here.
       float alpha = 1.f;
       bool rescale = false;
       if (j == 0) {
@@ -442,67 +433,70 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
         m = mxs;
         rescale = true;
       }
-      // P = exp2(s * scale_log2 - m) as bf16 pairs, computed while the previous
-      // tile's PV still runs on the tensor core.
       const float2 negm = make_float2(-m, -m);
-      uint32_t pk[kHalfCols / 2];
+      uint32_t pk[kBN / 2];
       float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int i = 0; i < kHalfCols / 2; ++i) {
-        const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scale2, negm);
-        const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+      for (int i = 0; i < kBN / 2; ++i) {
+        const float2 xx = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), scale2, negm);
+        const float2 p = make_float2(fast_exp2(xx.x), fast_exp2(xx.y));
         sum2 = __fadd2_rn(sum2, p);
         pk[i] = pack_bf16x2(p.x, p.y);
       }
-      if (j > 0) {
-        // PV of the previous tile has finished: O is stable and P is free.
-        if (!mbar_wait(&bars[B_ODONE], (jt - 1) & 1, a.status)) return;
-        tc_fence_after();
-        if (rescale) {
-          l *= alpha;
+      if (rescale) {  // S commit of this tile => the previous PV into O is complete
+        l *= alpha;
 #pragma unroll
-          for (int c = 0; c < kHalfD / 32; ++c) {
-            uint32_t v[32];
-            const uint32_t addr = tbase + lane_base + 2 * kBN + half * kHalfD + c * 32;
-            tmem_ld32(addr, v);
-            tmem_ld_wait();
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(o_col + c * 32, v);
+          tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float2 o = __fmul2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
-                                          make_float2(alpha, alpha));
-              v[i] = __float_as_uint(o.x);
-              v[i + 1] = __float_as_uint(o.y);
-            }
-            tmem_st32(addr, v);
+          for (int i = 0; i < 32; i += 2) {
+            const float2 o = __fmul2_rn(make_float2(__uint_as_float(v[i]), __uint_as_float(v[i + 1])),
+                                        make_float2(alpha, alpha));
+            v[i] = __float_as_uint(o.x);
+            v[i + 1] = __float_as_uint(o.y);
           }
-          tmem_st_wait();
+          tmem_st32(o_col + c * 32, v);
         }
+        tmem_st_wait();
       }
       l += sum2.x + sum2.y;
-      // P into shared memory, 128-byte swizzled K-major (the PV MMA's A
-      // operand): this thread's 64 keys are exactly 64-key panel `half`.
+      // The P buffer was last read by the PV issued just before this tile's:
+      // tile A waits for B's previous PV (or its own when B is absent), tile
+      // B waits for A's PV of the same kv tile.
+      if (x == 0) {
+        const bool wait_b = (j > 0) ? has_b : (!first && prev_has_b);
+        const bool wait_a = (j > 0) ? !has_b : (!first && !prev_has_b);
+        if (wait_b && !mbar_wait(&bars[B_PVDONE + 1], (npv[1] - 1) & 1, a.status)) return;
+        if (wait_a && !mbar_wait(&bars[B_PVDONE + 0], (npv[0] - 1) & 1, a.status)) return;
+      } else {
+        if (!mbar_wait(&bars[B_PVDONE + 0], npv[0] & 1, a.status)) return;
+      }
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(sP + half * Lay::kPanelBytes + r * 128 + ((c ^ (r & 7)) << 4)) =
+      for (int c = 0; c < kBN / 8; ++c) {
+        const int panel = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4*>(sP + panel * Lay::kPanelBytes + r * 128 + ((cc ^ (r & 7)) << 4)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_PFULL]);
-      iter_next(a, t);
+      if (lane == 0) mbar_arrive(&bars[B_PFULL + x]);
+      // PVs issued after this P: A's PV of this tile, then B's if present.
+      ++npv[0];
+      if (has_b) ++npv[1];
     }
-    // Epilogue: O / l -> bf16 -> out; each thread stores its half of the row.
-    if (!mbar_wait(&bars[B_ODONE], (t.jt - 1) & 1, a.status)) return;
+    // Epilogue: wait for this tile's last PV, O / l -> bf16 -> out.
+    if (!mbar_wait(&bars[B_PVDONE + x], (npv[x] - 1) & 1, a.status)) return;
     tc_fence_after();
-    float l_other;
-    if (!exchange(l, l_other)) return;
-    const float inv = 1.f / (l + l_other);
-    uint16_t* orow = a.out + (int64_t)(it.q_row0 + tok) * a.out_stride +
-                     (int64_t)(it.g * a.group + h) * D + half * kHalfD;
+    const float inv = 1.f / l;
+    uint16_t* orow = a.out + (int64_t)(it.q_row0 + x * a.tok_per_tile + tok) * a.out_stride +
+                     (int64_t)(it.g * a.group + h) * D;
 #pragma unroll
-    for (int c = 0; c < kHalfD / 32; ++c) {
+    for (int c = 0; c < D / 32; ++c) {
       uint32_t v[32];
-      tmem_ld32(tbase + lane_base + 2 * kBN + half * kHalfD + c * 32, v);
+      tmem_ld32(o_col + c * 32, v);
       tmem_ld_wait();
       if (row_valid) {
 #pragma unroll
@@ -518,7 +512,9 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bars[B_OFREE]);
+    if (lane == 0) mbar_arrive(&bars[B_OFREE + x]);
+    prev_has_b = has_b;
+    first = false;
   }
 }
 
@@ -538,24 +534,23 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
   const int warp = threadIdx.x >> 5;
 
   if (threadIdx.x == 0) {
+    mbar_init(&bars[B_QFULL], 1);
+    mbar_init(&bars[B_QEMPTY], 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[B_QFULL + i], 1);
-      mbar_init(&bars[B_QEMPTY + i], 1);
       mbar_init(&bars[B_KFULL + i], 1);
       mbar_init(&bars[B_KEMPTY + i], 1);
       mbar_init(&bars[B_VFULL + i], 1);
       mbar_init(&bars[B_VEMPTY + i], 1);
       mbar_init(&bars[B_SFULL + i], 1);
+      mbar_init(&bars[B_PFULL + i], 4);
+      mbar_init(&bars[B_PVDONE + i], 1);
+      mbar_init(&bars[B_OFREE + i], 4);
     }
-    mbar_init(&bars[B_PFULL], kSoftmaxWarps);
-    mbar_init(&bars[B_ODONE], 1);
-    mbar_init(&bars[B_OFREE], kSoftmaxWarps);
     mbar_init(&bars[B_DRAIN], 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&bars[B_XCH + i], 2);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(tmem_slot, 512);  // S0 | S1 | O (D columns)
+    tmem_alloc(tmem_slot, 512);  // S_A | S_B | O_A | O_B
     tmem_relinquish();
   }
   tc_fence_before();
@@ -563,12 +558,16 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp == kProducerWarp)
-    producer_role<D>(a, &tmQ, &tmK, &tmV, smem, bars);
-  else if (warp == kMmaWarp)
-    mma_role<D>(a, smem, bars, tbase);
-  else
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
+    if (warp == kProducerWarp)
+      producer_role<D>(a, &tmQ, &tmK, &tmV, smem, bars);
+    else if (warp == kMmaWarp)
+      mma_role<D>(a, smem, bars, tbase);
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     softmax_role<D>(a, smem, bars, tbase);
+  }
 
   tc_fence_before();
   __syncthreads();
@@ -676,12 +675,12 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
   a.group = G;
   a.tok_per_tile = tok;
   a.sub_rows = sub_rows;
-  a.max_tiles = (max_seqlen_q + tok - 1) / tok;
+  a.max_pairs = (max_seqlen_q + 2 * tok - 1) / (2 * tok);
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.out = out;
   a.out_stride = out_stride;
   a.status = status;
-  const long long items = (long long)a.max_tiles * num_seqs * num_kv_heads;
+  const long long items = (long long)a.max_pairs * num_seqs * num_kv_heads;
   if (items >= (1ll << 31)) {
     *why = "too many work items";
     return KVP_ERR_UNSUPPORTED;
