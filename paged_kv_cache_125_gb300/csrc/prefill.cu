@@ -79,6 +79,7 @@ struct PrefillArgs {
   int tok_per_tile;  // 128 / G
   int sub_rows;      // rows per TMA box of a kv tile (paged: min(bs, 128))
   int max_pairs;     // ceil(max_seqlen_q / (2 * tok_per_tile))
+  int use_list;      // 1: items dealt by the cost-sorted schedule; 0: round-robin
   float scale_log2;
   uint16_t* out;
   int64_t out_stride;
@@ -91,14 +92,13 @@ struct Layout {
   static constexpr uint32_t kPanelBytes = 128 * 128;  // 128 rows x 128 bytes
   static constexpr uint32_t kQBytes = kBM * D * 2;    // one query tile
   static constexpr uint32_t kKVBytes = kBN * D * 2;
-  static constexpr uint32_t kPBytes = kBM * kBN * 2;
   static constexpr uint32_t kQ = 0;                  // tiles A, B
   static constexpr uint32_t kK = kQ + 2 * kQBytes;   // 2 slots
   static constexpr uint32_t kV = kK + 2 * kKVBytes;  // 2 slots
-  static constexpr uint32_t kP = kV + 2 * kKVBytes;  // 1 buffer
-  static constexpr uint32_t kBar = kP + kPBytes;
+  static constexpr uint32_t kBar = kV + 2 * kKVBytes;
   static constexpr uint32_t kNumBars = 21;
-  static constexpr uint32_t kTotal = kBar + kNumBars * 8 + 16;
+  static constexpr uint32_t kSched = kBar + kNumBars * 8 + 16;
+  static constexpr uint32_t kTotal = kSched + 1024 + 16 + 128 * 4;
   // The dynamic shared memory base is 1 KiB aligned on this architecture (the
   // kernel checks it and reports KVP_ERR_DEVICE_DATA otherwise).
   static constexpr uint32_t kAlloc = kTotal + 128;
@@ -159,10 +159,112 @@ __device__ __forceinline__ int total_items(const PrefillArgs& a) {
   return a.max_pairs * a.num_seqs * a.num_kv_heads;
 }
 
-// Next item of this CTA at or after index L (items are dealt round-robin).
-__device__ __forceinline__ bool next_item(const PrefillArgs& a, int& L, Item& it) {
-  for (; L < total_items(a); L += gridDim.x)
+// Per-CTA work list.  An item's cost (kv tiles x query tiles) depends only on
+// its sequence and pair rank, not on the kv head, so the schedule is built
+// over (rank, sequence) pairs: every CTA computes the same cost histogram,
+// ranks the pairs by cost (ties in index order), and keeps the items that a
+// snake deal of the sorted list (0..P-1, P-1..0, ...) gives it.  Greedy on the
+// sorted order keeps the heaviest SM close to the average.
+constexpr int kCostBins = 256;
+constexpr int kMaxListItems = 128;
+
+struct Sched {
+  uint32_t bins[kCostBins];  // histogram, then next free position per cost
+  int count;
+  int pad[3];
+  int items[kMaxListItems];
+};
+static_assert(sizeof(Sched) == 1024 + 16 + 128 * 4, "Sched size matches the layout");
+
+__device__ __forceinline__ bool pair_cost(const PrefillArgs& a, int idx, int& v) {
+  const int r = idx / a.num_seqs, b = idx - r * a.num_seqs;
+  const int q_len = a.cu_q[b + 1] - a.cu_q[b];
+  const int k_len = a.cu_k[b + 1] - a.cu_k[b];
+  if (q_len <= 0 || k_len < q_len) return false;
+  const int span = 2 * a.tok_per_tile;
+  const int npairs = (q_len + span - 1) / span;
+  if (r >= npairs) return false;
+  const int q0 = (npairs - 1 - r) * span;
+  const int rows_a = min(a.tok_per_tile, q_len - q0);
+  const int rows_b = max(0, min(a.tok_per_tile, q_len - q0 - a.tok_per_tile));
+  const int n_tiles = (k_len - q_len + q0 + rows_a + rows_b + kBN - 1) / kBN;
+  v = min(kCostBins - 1, n_tiles * (rows_b > 0 ? 2 : 1) + 1);
+  return true;
+}
+
+// Built by one warp before the roles start.
+__device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
+  const int lane = threadIdx.x & 31;
+  const int H = a.num_kv_heads, P = gridDim.x;
+  const int npi = a.max_pairs * a.num_seqs;
+  for (int i = lane; i < kCostBins; i += 32) sc->bins[i] = 0;
+  if (lane == 0) sc->count = 0;
+  __syncwarp();
+  for (int idx = lane; idx < npi; idx += 32) {
+    int v;
+    if (pair_cost(a, idx, v)) atomicAdd(&sc->bins[v], (uint32_t)H);
+  }
+  __syncwarp();
+  // Exclusive prefix in descending cost: lane 0 owns the 8 highest bins.
+  const int base = (31 - lane) * 8;
+  uint32_t sum = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) sum += sc->bins[base + k];
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t run = incl - sum;
+  __syncwarp();
+#pragma unroll
+  for (int k = 7; k >= 0; --k) {
+    const uint32_t c = sc->bins[base + k];
+    sc->bins[base + k] = run;
+    run += c;
+  }
+  __syncwarp();
+  // Positions in (rank, sequence) order; equal costs keep index order.
+  for (int b0 = 0; b0 < npi; b0 += 32) {
+    const int idx = b0 + lane;
+    int v = -1;
+    const bool ok = idx < npi && pair_cost(a, idx, v);
+    const unsigned same = __match_any_sync(0xffffffffu, ok ? v : -1);
+    const unsigned lower = same & ((1u << lane) - 1u);
+    uint32_t pos0 = 0;
+    if (ok) pos0 = sc->bins[v] + (uint32_t)__popc(lower) * H;
+    __syncwarp();
+    if (ok && lower == 0) sc->bins[v] += (uint32_t)__popc(same) * H;
+    if (ok) {
+      for (int g = 0; g < H; ++g) {
+        const uint32_t p = pos0 + g;
+        const int round = p / P, j = p - round * P;
+        const int cta = (round & 1) ? P - 1 - j : j;
+        if (cta == (int)blockIdx.x) {
+          const int slot = atomicAdd(&sc->count, 1);
+          if (slot < kMaxListItems) sc->items[slot] = idx * H + g;
+        }
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// Next item of this CTA: from the work list, or round-robin over all items.
+// `cursor` starts at 0 and is advanced past the returned item.
+__device__ __forceinline__ bool next_item(const PrefillArgs& a, const Sched* sc, int& cursor,
+                                          Item& it) {
+  if (a.use_list) {
+    const int n = min(sc->count, kMaxListItems);
+    while (cursor < n)
+      if (decode_item(a, sc->items[cursor++], it)) return true;
+    return false;
+  }
+  for (int L = blockIdx.x + cursor * (int)gridDim.x; L < total_items(a); L += gridDim.x) {
+    ++cursor;
     if (decode_item(a, L, it)) return true;
+  }
   return false;
 }
 
@@ -176,7 +278,8 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 template <int D>
 __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                              const CUtensorMap* tmV, uint8_t* smem, uint64_t* bars) {
+                              const CUtensorMap* tmV, uint8_t* smem, uint64_t* bars,
+                              const Sched* sc) {
   using Lay = Layout<D>;
   const int lane = threadIdx.x & 31;
   if (lane == 0) {
@@ -187,7 +290,7 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
   int item_idx = 0;
   uint32_t jt = 0;
   Item it;
-  for (int L = blockIdx.x; next_item(a, L, it); L += gridDim.x, ++item_idx) {
+  for (int cur = 0; next_item(a, sc, cur, it); ++item_idx) {
     // Q pair: both tiles in one slot (tile B past the sequence is harmless
     // data: its rows are never stored).
     if (!mbar_wait(&bars[B_QEMPTY], (item_idx & 1) ^ 1u, a.status)) return;
@@ -267,31 +370,32 @@ __device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint32_t qa, uint32_t ka
   }
 }
 
+// O (+)= P V with P read from tensor memory (bf16 pairs written by the
+// softmax warps over the first 64 columns of the tile's S region).
 template <int D>
-__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t pa, uint32_t va, bool acc) {
+__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t va, bool acc) {
   using Lay = Layout<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, 0, 1);
 #pragma unroll
   for (int kk = 0; kk < kBN / 16; ++kk) {
-    const uint64_t ad = smem_desc(pa + (kk >> 2) * Lay::kPanelBytes + (kk & 3) * 32, 16, 1024, 2);
     const uint64_t bd = smem_desc(va + kk * 16 * 128, Lay::kPanelBytes, 1024, 2);
-    umma_f16_ss(d_tmem, ad, bd, idesc, (acc || kk > 0) ? 1u : 0u);
+    umma_f16_ts(d_tmem, p_tmem + kk * 8, bd, idesc, (acc || kk > 0) ? 1u : 0u);
   }
 }
 
 template <int D>
-__device__ void mma_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, uint32_t tbase) {
+__device__ void mma_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, uint32_t tbase,
+                         const Sched* sc) {
   using Lay = Layout<D>;
   const int lane = threadIdx.x & 31;
   const uint32_t qa[2] = {smem_u32(smem + Lay::kQ), smem_u32(smem + Lay::kQ + Lay::kQBytes)};
-  const uint32_t pa = smem_u32(smem + Lay::kP);
   uint32_t ns[2] = {0, 0};    // S issued per tile
   uint32_t np[2] = {0, 0};    // P consumed (PV issued) per tile
   uint32_t nitems[2] = {0, 0};  // items per tile (A: all, B: those with rows)
   int item_idx = 0;
   uint32_t jt = 0;
   Item it;
-  for (int L = blockIdx.x; next_item(a, L, it); L += gridDim.x, ++item_idx) {
+  for (int cur = 0; next_item(a, sc, cur, it); ++item_idx) {
     const bool has_b = it.rows_b > 0;
     const int ntile = has_b ? 2 : 1;
     if (!mbar_wait(&bars[B_QFULL], item_idx & 1, a.status)) goto drain;
@@ -334,7 +438,7 @@ __device__ void mma_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, ui
           goto drain;
         tc_fence_after();
         if (lane == 0) {
-          mma_pv<D>(tbase + 2 * kBN + x * kBN, pa, smem_u32(vs), j > 0);
+          mma_pv<D>(tbase + 2 * kBN + x * kBN, tbase + x * kBN, smem_u32(vs), j > 0);
           umma_commit(&bars[B_PVDONE + x]);
         }
         __syncwarp();
@@ -369,7 +473,8 @@ drain:
 // ------------------------------------------------------------------ softmax
 
 template <int D>
-__device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, uint32_t tbase) {
+__device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, uint32_t tbase,
+                             const Sched* sc) {
   using Lay = Layout<D>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int x = warp >> 2;               // query tile: 0 = A, 1 = B
@@ -377,21 +482,14 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
   const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
   const uint32_t s_col = tbase + lane_base + x * kBN;
   const uint32_t o_col = tbase + lane_base + 2 * kBN + x * kBN;
-  uint8_t* sP = smem + Lay::kP;
   const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
-  uint32_t ns = 0;                 // S tiles consumed by this tile's warpgroup
-  uint32_t npv[2] = {0, 0};        // PVs of tiles A / B that this thread has seen issued
-  bool prev_has_b = false, first = true;
+  uint32_t ns = 0;   // S tiles consumed by this tile's warpgroup
+  uint32_t npv = 0;  // PVs of this tile issued after this warpgroup's P writes
   Item it;
-  for (int L = blockIdx.x; next_item(a, L, it); L += gridDim.x) {
+  for (int cur = 0; next_item(a, sc, cur, it);) {
     const bool has_b = it.rows_b > 0;
     const int rows = x == 0 ? it.rows_a : it.rows_b;
-    if (x == 1 && !has_b) {
-      npv[0] += it.n_tiles;
-      prev_has_b = false;
-      first = false;
-      continue;
-    }
+    if (x == 1 && !has_b) continue;
     const int tok = r / a.group, h = r - tok * a.group;
     const bool row_valid = tok < rows;
     const int tok0 = it.q0 + x * a.tok_per_tile;  // first token of this tile
@@ -401,15 +499,16 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
       if (!mbar_wait(&bars[B_SFULL + x], ns & 1, a.status)) return;
       ++ns;
       tc_fence_after();
+      // All four 32-column loads in flight, one wait.
+      uint32_t sv[kBN / 32][32];
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) tmem_ld32(s_col + c * 32, sv[c]);
+      tmem_ld_wait();
       float s[kBN];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(s_col + c * 32, v);
-        tmem_ld_wait();
+      for (int c = 0; c < kBN / 32; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
-      }
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sv[c][i]);
       const int lim = pos - j * kBN;  // columns <= lim are visible
       if (lim < kBN - 1) {
 #pragma unroll
@@ -462,33 +561,25 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
         tmem_st_wait();
       }
       l += sum2.x + sum2.y;
-      // The P buffer was last read by the PV issued just before this tile's:
-      // tile A waits for B's previous PV (or its own when B is absent), tile
-      // B waits for A's PV of the same kv tile.
-      if (x == 0) {
-        const bool wait_b = (j > 0) ? has_b : (!first && prev_has_b);
-        const bool wait_a = (j > 0) ? !has_b : (!first && !prev_has_b);
-        if (wait_b && !mbar_wait(&bars[B_PVDONE + 1], (npv[1] - 1) & 1, a.status)) return;
-        if (wait_a && !mbar_wait(&bars[B_PVDONE + 0], (npv[0] - 1) & 1, a.status)) return;
-      } else {
-        if (!mbar_wait(&bars[B_PVDONE + 0], npv[0] & 1, a.status)) return;
-      }
+      // P (bf16 pairs) into the first 64 columns of this tile's S region, where
+      // the PV MMA reads it as its A operand.  The S columns are free: this
+      // thread has read them, and the next S of this tile is issued only after
+      // the PV that reads this P.
 #pragma unroll
-      for (int c = 0; c < kBN / 8; ++c) {
-        const int panel = c >> 3, cc = c & 7;
-        *reinterpret_cast<uint4*>(sP + panel * Lay::kPanelBytes + r * 128 + ((cc ^ (r & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+      for (int c = 0; c < kBN / 64; ++c) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = pk[c * 32 + i];
+        tmem_st32(s_col + c * 32, w);
       }
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_PFULL + x]);
-      // PVs issued after this P: A's PV of this tile, then B's if present.
-      ++npv[0];
-      if (has_b) ++npv[1];
+      ++npv;
     }
     // Epilogue: wait for this tile's last PV, O / l -> bf16 -> out.
-    if (!mbar_wait(&bars[B_PVDONE + x], (npv[x] - 1) & 1, a.status)) return;
+    if (!mbar_wait(&bars[B_PVDONE + x], (npv - 1) & 1, a.status)) return;
     tc_fence_after();
     const float inv = 1.f / l;
     uint16_t* orow = a.out + (int64_t)(it.q_row0 + x * a.tok_per_tile + tok) * a.out_stride +
@@ -513,8 +604,6 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[B_OFREE + x]);
-    prev_has_b = has_b;
-    first = false;
   }
 }
 
@@ -531,7 +620,9 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
   uint8_t* smem = smem_raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Lay::kNumBars);
+  Sched* sc = reinterpret_cast<Sched*>(smem + Lay::kSched);
   const int warp = threadIdx.x >> 5;
+  if (warp == kProducerWarp && a.use_list) build_schedule(a, sc);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_QFULL], 1);
@@ -561,12 +652,12 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
     if (warp == kProducerWarp)
-      producer_role<D>(a, &tmQ, &tmK, &tmV, smem, bars);
+      producer_role<D>(a, &tmQ, &tmK, &tmV, smem, bars, sc);
     else if (warp == kMmaWarp)
-      mma_role<D>(a, smem, bars, tbase);
+      mma_role<D>(a, smem, bars, tbase, sc);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
-    softmax_role<D>(a, smem, bars, tbase);
+    softmax_role<D>(a, smem, bars, tbase, sc);
   }
 
   tc_fence_before();
@@ -686,6 +777,7 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
     return KVP_ERR_UNSUPPORTED;
   }
   const int grid = (int)(items < num_sms ? items : num_sms);
+  a.use_list = items <= (long long)128 * grid ? 1 : 0;
   cudaError_t e = head_dim == 128 ? launch_t<128>(mq, mk, mv, a, grid, stream)
                                   : launch_t<64>(mq, mk, mv, a, grid, stream);
   if (e != cudaSuccess) {
