@@ -45,7 +45,10 @@ N_SETS = 4
 # measured on; a figure whose source has changed since is reported as null.
 TRAFFIC = {
     "decode": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu", "sha256": None, "bytes": None},
-    "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu", "sha256": None, "bytes": None},
+    # prefill workload (8 prompts, 32/8/128), one ncu --set full capture
+    "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
+                "sha256": "494c03c9ff99f497252379b3894f407538f2e476775e16d3395f75fbf4d31598",
+                "bytes": 121241088 + 28700672},
 }
 
 
@@ -489,7 +492,13 @@ def run_ours(args, rank, world, local):
                        "l2": f"{args.sets} input sets in rotation ({dec['footprint_gb']:.1f} GB of pools) vs 126 MB L2",
                        "graph": "each step is two CUDA graph replays (store, attention)"},
             "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
-            "gpu_launches": 3 * args.steps, "clocks": clocks,
+            "gpu_launches": 3 * args.steps + (0 if pre is None else 2 * pre["line"]["steps"]),
+            "gpu_launches_by_region": {"decode": {"kv_store": args.steps, "decode_split": args.steps,
+                                                  "decode_merge": args.steps},
+                                       "prefill": None if pre is None else
+                                       {"kv_store": pre["line"]["steps"],
+                                        "prefill": pre["line"]["steps"]}},
+            "clocks": clocks,
             "prefill": None if pre is None else pre["line"]}
     print(json.dumps(line), flush=True)
 

@@ -58,6 +58,7 @@ constexpr int kBN = 128;  // keys per kv tile
 constexpr int kThreadsPF = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kVFixWarp = 10;
 constexpr int kSoftmaxRegs = 200;
 constexpr int kControlRegs = 104;
 static_assert(128 * (2 * kSoftmaxRegs + kControlRegs) <= kThreadsPF * 168,
@@ -80,11 +81,34 @@ struct PrefillArgs {
   int sub_rows;      // rows per TMA box of a kv tile (paged: min(bs, 128))
   int max_pairs;     // ceil(max_seqlen_q / (2 * tok_per_tile))
   int use_list;      // 1: items dealt by the cost-sorted schedule; 0: round-robin
+  int cu_in_smem;    // 1: cu_seqlens_q/k are copied into shared memory at kernel start
   float scale_log2;
   uint16_t* out;
   int64_t out_stride;
   int* status;
 };
+
+struct Item {
+  int b, g, q0, q_len, cached, k_len, n_tiles;
+  int rows_a, rows_b;  // valid tokens in tile A / B (rows_b may be 0)
+  int q_row0;          // packed row of tile A's first token
+  int k_row0;          // packed row of the sequence's first key (packed mode)
+};
+
+constexpr int kCostBins = 256;
+constexpr int kMaxListItems = 128;
+constexpr int kCuCap = 520;  // cu_seqlens entries cached in shared memory (num_seqs + 1)
+
+// Per-CTA schedule state in shared memory (written before the roles start).
+struct Sched {
+  uint32_t bins[kCostBins];  // histogram, then next free position per cost
+  int count;
+  int pad[3];
+  int items[kMaxListItems];   // item indices dealt to this CTA
+  Item list[kMaxListItems];   // the same items, decoded
+  int cu[2][kCuCap];          // cu_seqlens_q, cu_seqlens_k
+};
+constexpr uint32_t kSchedBytes = (sizeof(Sched) + 15) & ~15u;
 
 template <int D>
 struct Layout {
@@ -98,7 +122,7 @@ struct Layout {
   static constexpr uint32_t kBar = kV + 2 * kKVBytes;
   static constexpr uint32_t kNumBars = 21;
   static constexpr uint32_t kSched = kBar + kNumBars * 8 + 16;
-  static constexpr uint32_t kTotal = kSched + 1024 + 16 + 128 * 4;
+  static constexpr uint32_t kTotal = kSched + kSchedBytes;
   // The dynamic shared memory base is 1 KiB aligned on this architecture (the
   // kernel checks it and reports KVP_ERR_DEVICE_DATA otherwise).
   static constexpr uint32_t kAlloc = kTotal + 128;
@@ -116,24 +140,29 @@ enum : int {
   B_PFULL = 12,  // [2]
   B_PVDONE = 14, // [2]
   B_OFREE = 16,  // [2]
-  B_DRAIN = 18,
+  B_VREADY = 18, // [2]: V tile loaded and its rows past the last key zeroed
+  B_DRAIN = 20,
 };
 
-struct Item {
-  int b, g, q0, q_len, cached, k_len, n_tiles;
-  int rows_a, rows_b;  // valid tokens in tile A / B (rows_b may be 0)
-  int q_row0;          // packed row of tile A's first token
-  int k_row0;          // packed row of the sequence's first key (packed mode)
+// cu_seqlens as the roles read them: from shared memory when cached there.
+struct Cu {
+  const int* q;
+  const int* k;
 };
 
-__device__ __forceinline__ bool decode_item(const PrefillArgs& a, int L, Item& it) {
+__device__ __forceinline__ Cu cu_view(const PrefillArgs& a, const Sched* sc) {
+  if (a.cu_in_smem) return Cu{sc->cu[0], sc->cu[1]};
+  return Cu{a.cu_q, a.cu_k};
+}
+
+__device__ __forceinline__ bool decode_item(const PrefillArgs& a, const Cu& cu, int L, Item& it) {
   const int per_r = a.num_seqs * a.num_kv_heads;
   const int r = L / per_r;
   const int rem = L - r * per_r;
   it.b = rem / a.num_kv_heads;
   it.g = rem - it.b * a.num_kv_heads;
-  const int cq0 = a.cu_q[it.b], cq1 = a.cu_q[it.b + 1];
-  const int ck0 = a.cu_k[it.b], ck1 = a.cu_k[it.b + 1];
+  const int cq0 = cu.q[it.b], cq1 = cu.q[it.b + 1];
+  const int ck0 = cu.k[it.b], ck1 = cu.k[it.b + 1];
   it.q_len = cq1 - cq0;
   it.k_len = ck1 - ck0;
   if (it.q_len <= 0 || it.k_len < it.q_len) {
@@ -165,22 +194,14 @@ __device__ __forceinline__ int total_items(const PrefillArgs& a) {
 // ranks the pairs by cost (ties in index order), and keeps the items that a
 // snake deal of the sorted list (0..P-1, P-1..0, ...) gives it.  Greedy on the
 // sorted order keeps the heaviest SM close to the average.
-constexpr int kCostBins = 256;
-constexpr int kMaxListItems = 128;
-
-struct Sched {
-  uint32_t bins[kCostBins];  // histogram, then next free position per cost
-  int count;
-  int pad[3];
-  int items[kMaxListItems];
-};
-static_assert(sizeof(Sched) == 1024 + 16 + 128 * 4, "Sched size matches the layout");
-
-__device__ __forceinline__ bool pair_cost(const PrefillArgs& a, int idx, int& v) {
+__device__ __forceinline__ bool pair_cost(const PrefillArgs& a, const Cu& cu, int idx, int& v) {
   const int r = idx / a.num_seqs, b = idx - r * a.num_seqs;
-  const int q_len = a.cu_q[b + 1] - a.cu_q[b];
-  const int k_len = a.cu_k[b + 1] - a.cu_k[b];
-  if (q_len <= 0 || k_len < q_len) return false;
+  const int q_len = cu.q[b + 1] - cu.q[b];
+  const int k_len = cu.k[b + 1] - cu.k[b];
+  if (q_len <= 0 || k_len < q_len) {
+    if (q_len > 0 && r == 0) record_error(a.status, KVP_ERR_DEVICE_DATA);
+    return false;
+  }
   const int span = 2 * a.tok_per_tile;
   const int npairs = (q_len + span - 1) / span;
   if (r >= npairs) return false;
@@ -192,9 +213,19 @@ __device__ __forceinline__ bool pair_cost(const PrefillArgs& a, int idx, int& v)
   return true;
 }
 
-// Built by one warp before the roles start.
+// Built by one warp before the roles start: cu_seqlens into shared memory,
+// the cost-sorted deal, then the dealt items decoded.
 __device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
   const int lane = threadIdx.x & 31;
+  if (a.cu_in_smem) {
+    for (int i = lane; i <= a.num_seqs; i += 32) {
+      sc->cu[0][i] = a.cu_q[i];
+      sc->cu[1][i] = a.cu_k[i];
+    }
+    __syncwarp();
+  }
+  if (!a.use_list) return;
+  const Cu cu = cu_view(a, sc);
   const int H = a.num_kv_heads, P = gridDim.x;
   const int npi = a.max_pairs * a.num_seqs;
   for (int i = lane; i < kCostBins; i += 32) sc->bins[i] = 0;
@@ -202,7 +233,7 @@ __device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
   __syncwarp();
   for (int idx = lane; idx < npi; idx += 32) {
     int v;
-    if (pair_cost(a, idx, v)) atomicAdd(&sc->bins[v], (uint32_t)H);
+    if (pair_cost(a, cu, idx, v)) atomicAdd(&sc->bins[v], (uint32_t)H);
   }
   __syncwarp();
   // Exclusive prefix in descending cost: lane 0 owns the 8 highest bins.
@@ -229,7 +260,7 @@ __device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
   for (int b0 = 0; b0 < npi; b0 += 32) {
     const int idx = b0 + lane;
     int v = -1;
-    const bool ok = idx < npi && pair_cost(a, idx, v);
+    const bool ok = idx < npi && pair_cost(a, cu, idx, v);
     const unsigned same = __match_any_sync(0xffffffffu, ok ? v : -1);
     const unsigned lower = same & ((1u << lane) - 1u);
     uint32_t pos0 = 0;
@@ -249,6 +280,9 @@ __device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
     }
     __syncwarp();
   }
+  const int n = min(sc->count, kMaxListItems);
+  for (int i = lane; i < n; i += 32) decode_item(a, cu, sc->items[i], sc->list[i]);
+  __syncwarp();
 }
 
 // Next item of this CTA: from the work list, or round-robin over all items.
@@ -256,14 +290,14 @@ __device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
 __device__ __forceinline__ bool next_item(const PrefillArgs& a, const Sched* sc, int& cursor,
                                           Item& it) {
   if (a.use_list) {
-    const int n = min(sc->count, kMaxListItems);
-    while (cursor < n)
-      if (decode_item(a, sc->items[cursor++], it)) return true;
-    return false;
+    if (cursor >= min(sc->count, kMaxListItems)) return false;
+    it = sc->list[cursor++];
+    return true;
   }
+  const Cu cu = cu_view(a, sc);
   for (int L = blockIdx.x + cursor * (int)gridDim.x; L < total_items(a); L += gridDim.x) {
     ++cursor;
-    if (decode_item(a, L, it)) return true;
+    if (decode_item(a, cu, L, it)) return true;
   }
   return false;
 }
@@ -358,71 +392,118 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
 
 // ------------------------------------------------------------------ MMA issuer
 
+// S = Q K^T for one query tile: D/16 K-steps of M128 N128 K16.  `dq`, `dk`
+// are the descriptors of the tiles' first panels; a K-step moves 32 bytes
+// inside a 128-byte swizzled row, and every 4 K-steps the next 64-column panel.
 template <int D>
-__device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint32_t qa, uint32_t ka) {
+__device__ __forceinline__ void mma_qk(uint32_t d_tmem, uint64_t dq, uint64_t dk) {
   using Lay = Layout<D>;
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, kBN, 0, 0);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (kk >> 2) * Lay::kPanelBytes + (kk & 3) * 32;
-    umma_f16_ss(d_tmem, smem_desc(qa + off, 16, 1024, 2), smem_desc(ka + off, 16, 1024, 2), idesc,
-                kk > 0);
+    const uint32_t off = ((kk >> 2) * Lay::kPanelBytes + (kk & 3) * 32) >> 4;
+    umma_f16_ss(d_tmem, dq + off, dk + off, idesc, kk > 0);
   }
 }
 
 // O (+)= P V with P read from tensor memory (bf16 pairs written by the
-// softmax warps over the first 64 columns of the tile's S region).
+// softmax warps over the first 64 columns of the tile's S region).  V is the
+// MN-major B operand: a K-step is 16 key rows (2 KiB).
 template <int D>
-__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t va, bool acc) {
-  using Lay = Layout<D>;
+__device__ __forceinline__ void mma_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t dv, bool acc) {
   constexpr uint32_t idesc = idesc_bf16_f32(kBM, D, 0, 1);
 #pragma unroll
-  for (int kk = 0; kk < kBN / 16; ++kk) {
-    const uint64_t bd = smem_desc(va + kk * 16 * 128, Lay::kPanelBytes, 1024, 2);
-    umma_f16_ts(d_tmem, p_tmem + kk * 8, bd, idesc, (acc || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < kBN / 16; ++kk)
+    umma_f16_ts(d_tmem, p_tmem + kk * 8, dv + ((kk * 16 * 128) >> 4), idesc,
+                (acc || kk > 0) ? 1u : 0u);
 }
 
+// The MMA issuer: one thread.  tcgen05.mma issue keeps pace with execution
+// (the queue in front of the tensor core is short), so anything this thread
+// does between two batches of MMAs is idle tensor time.  It therefore waits
+// for all inputs of a tile step first and then issues PV and the next S of
+// the tile back to back; shared-memory fix-ups of V are done by another warp.
 template <int D>
 __device__ void mma_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, uint32_t tbase,
                          const Sched* sc) {
   using Lay = Layout<D>;
-  const int lane = threadIdx.x & 31;
-  const uint32_t qa[2] = {smem_u32(smem + Lay::kQ), smem_u32(smem + Lay::kQ + Lay::kQBytes)};
-  uint32_t ns[2] = {0, 0};    // S issued per tile
-  uint32_t np[2] = {0, 0};    // P consumed (PV issued) per tile
+  // Descriptors of the first Q tile, K slot and V slot; the others are at
+  // fixed byte offsets, added to the address field (bytes >> 4).
+  const uint64_t dq0 = smem_desc(smem_u32(smem + Lay::kQ), 16, 1024, 2);
+  const uint64_t dk0 = smem_desc(smem_u32(smem + Lay::kK), 16, 1024, 2);
+  const uint64_t dv0 = smem_desc(smem_u32(smem + Lay::kV), Lay::kPanelBytes, 1024, 2);
+  constexpr uint32_t kQStep = Lay::kQBytes >> 4, kSlotStep = Lay::kKVBytes >> 4;
+  uint32_t np[2] = {0, 0};      // PVs issued per tile
   uint32_t nitems[2] = {0, 0};  // items per tile (A: all, B: those with rows)
   int item_idx = 0;
   uint32_t jt = 0;
   Item it;
   for (int cur = 0; next_item(a, sc, cur, it); ++item_idx) {
-    const bool has_b = it.rows_b > 0;
-    const int ntile = has_b ? 2 : 1;
+    const int ntile = it.rows_b > 0 ? 2 : 1;
     if (!mbar_wait(&bars[B_QFULL], item_idx & 1, a.status)) goto drain;
-    // S for kv tile 0
     if (!mbar_wait(&bars[B_KFULL + (jt & 1)], (jt >> 1) & 1, a.status)) goto drain;
     tc_fence_after();
-    if (lane == 0) {
-      const uint32_t ka = smem_u32(smem + Lay::kK + (jt & 1) * Lay::kKVBytes);
-      for (int x = 0; x < ntile; ++x) {
-        mma_qk<D>(tbase + x * kBN, qa[x], ka);
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+      if (x < ntile) {
+        mma_qk<D>(tbase + x * kBN, dq0 + x * kQStep, dk0 + (jt & 1) * kSlotStep);
         umma_commit(&bars[B_SFULL + x]);
       }
-      umma_commit(&bars[B_KEMPTY + (jt & 1)]);
-      if (it.n_tiles == 1) umma_commit(&bars[B_QEMPTY]);
     }
-    __syncwarp();
-    for (int x = 0; x < ntile; ++x) ++ns[x];
     for (int j = 0; j < it.n_tiles; ++j, ++jt) {
       const int st = jt & 1;
       const bool more = j + 1 < it.n_tiles;
       const uint32_t jn = jt + 1;
-      if (!mbar_wait(&bars[B_VFULL + st], (jt >> 1) & 1, a.status)) goto drain;
-      uint8_t* vs = smem + Lay::kV + st * Lay::kKVBytes;
-      // Rows past the sequence's last key may hold stale or poisoned data;
-      // P is 0 there, but 0 * NaN is NaN inside the MMA: zero them.
+      if (!mbar_wait(&bars[B_VREADY + st], (jt >> 1) & 1, a.status)) goto drain;
+      if (more && !mbar_wait(&bars[B_KFULL + (jn & 1)], (jn >> 1) & 1, a.status)) goto drain;
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (x < ntile) {
+          if (!mbar_wait(&bars[B_PFULL + x], np[x] & 1, a.status)) goto drain;
+          if (j == 0 && nitems[x] > 0 &&
+              !mbar_wait(&bars[B_OFREE + x], (nitems[x] - 1) & 1, a.status))
+            goto drain;
+          tc_fence_after();
+          mma_pv<D>(tbase + (2 + x) * kBN, tbase + x * kBN, dv0 + st * kSlotStep, j > 0);
+          if (more) {
+            mma_qk<D>(tbase + x * kBN, dq0 + x * kQStep, dk0 + (jn & 1) * kSlotStep);
+            umma_commit(&bars[B_SFULL + x]);
+          }
+          ++np[x];
+        }
+      }
+      if (!more) {  // the item's O tiles are final
+        umma_commit(&bars[B_PVDONE]);
+        if (ntile == 2) umma_commit(&bars[B_PVDONE + 1]);
+      }
+    }
+    ++nitems[0];
+    if (ntile == 2) ++nitems[1];
+  }
+drain:
+  // Every MMA this thread issued has completed before the CTA tears down.
+  umma_commit(&bars[B_DRAIN]);
+  mbar_wait(&bars[B_DRAIN], 0, a.status);
+}
+
+// V fix-up warp: waits for each V tile and, in paged mode, zeroes the rows
+// past the sequence's last key before the MMA may read the tile.  Those rows
+// hold whatever the physical block or an earlier tile left there; P is 0 for
+// them, but 0 * NaN is NaN inside the MMA.  (Packed mode loads whole boxes:
+// rows past the sequence belong to the next one or are filled with zeros.)
+template <int D>
+__device__ void vfix_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, const Sched* sc) {
+  using Lay = Layout<D>;
+  const int lane = threadIdx.x & 31;
+  uint32_t jt = 0;
+  Item it;
+  for (int cur = 0; next_item(a, sc, cur, it);) {
+    for (int j = 0; j < it.n_tiles; ++j, ++jt) {
+      const int st = jt & 1;
+      if (!mbar_wait(&bars[B_VFULL + st], (jt >> 1) & 1, a.status)) return;
       const int valid_rows = it.k_len - j * kBN;
-      if (valid_rows < kBN) {
+      if (a.paged && valid_rows < kBN) {
+        uint8_t* vs = smem + Lay::kV + st * Lay::kKVBytes;
         const int r0 = valid_rows < 0 ? 0 : valid_rows;
         const int n16 = (kBN - r0) * 8;
         for (int p = 0; p < (int)Lay::kPanels; ++p)
@@ -430,44 +511,11 @@ __device__ void mma_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, ui
             *reinterpret_cast<uint4*>(vs + p * Lay::kPanelBytes + r0 * 128 + i * 16) =
                 make_uint4(0, 0, 0, 0);
         fence_proxy_async_smem();
-        __syncwarp();
-      }
-      for (int x = 0; x < ntile; ++x) {
-        if (!mbar_wait(&bars[B_PFULL + x], np[x] & 1, a.status)) goto drain;
-        if (j == 0 && nitems[x] > 0 && !mbar_wait(&bars[B_OFREE + x], (nitems[x] - 1) & 1, a.status))
-          goto drain;
-        tc_fence_after();
-        if (lane == 0) {
-          mma_pv<D>(tbase + 2 * kBN + x * kBN, tbase + x * kBN, smem_u32(vs), j > 0);
-          umma_commit(&bars[B_PVDONE + x]);
-        }
-        __syncwarp();
-        if (more) {
-          if (!mbar_wait(&bars[B_KFULL + (jn & 1)], (jn >> 1) & 1, a.status)) goto drain;
-          tc_fence_after();
-          if (lane == 0) {
-            mma_qk<D>(tbase + x * kBN, qa[x], smem_u32(smem + Lay::kK + (jn & 1) * Lay::kKVBytes));
-            umma_commit(&bars[B_SFULL + x]);
-          }
-          __syncwarp();
-        }
-        ++np[x];
-        if (more) ++ns[x];
-      }
-      if (lane == 0) {
-        umma_commit(&bars[B_VEMPTY + st]);
-        if (more) umma_commit(&bars[B_KEMPTY + (jn & 1)]);
-        if (j + 2 == it.n_tiles) umma_commit(&bars[B_QEMPTY]);
       }
       __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_VREADY + st]);
     }
-    for (int x = 0; x < ntile; ++x) ++nitems[x];
   }
-drain:
-  // Every MMA this thread issued has completed before the CTA tears down.
-  if (lane == 0) umma_commit(&bars[B_DRAIN]);
-  __syncwarp();
-  mbar_wait(&bars[B_DRAIN], 0, a.status);
 }
 
 // ------------------------------------------------------------------ softmax
@@ -483,13 +531,19 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
   const uint32_t s_col = tbase + lane_base + x * kBN;
   const uint32_t o_col = tbase + lane_base + 2 * kBN + x * kBN;
   const float2 scale2 = make_float2(a.scale_log2, a.scale_log2);
-  uint32_t ns = 0;   // S tiles consumed by this tile's warpgroup
-  uint32_t npv = 0;  // PVs of this tile issued after this warpgroup's P writes
+  uint32_t ns = 0;    // S tiles consumed by this tile's warpgroup
+  uint32_t nit = 0;   // items this warpgroup took part in
+  uint32_t jt0 = 0;   // kv tiles of all earlier items (ring slot of tile j = (jt0 + j) & 1)
+  // The warpgroup of an item's last query tile releases the K, V and Q slots:
+  // it observes S of that tile complete, and that MMA was issued after every
+  // earlier MMA that read those slots.
+  const bool releaser = (warp & 3) == 0 && lane == 0;
   Item it;
-  for (int cur = 0; next_item(a, sc, cur, it);) {
+  for (int cur = 0; next_item(a, sc, cur, it); jt0 += it.n_tiles) {
     const bool has_b = it.rows_b > 0;
     const int rows = x == 0 ? it.rows_a : it.rows_b;
     if (x == 1 && !has_b) continue;
+    const bool last = x == (has_b ? 1 : 0);
     const int tok = r / a.group, h = r - tok * a.group;
     const bool row_valid = tok < rows;
     const int tok0 = it.q0 + x * a.tok_per_tile;  // first token of this tile
@@ -498,6 +552,11 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
     for (int j = 0; j < it.n_tiles; ++j) {
       if (!mbar_wait(&bars[B_SFULL + x], ns & 1, a.status)) return;
       ++ns;
+      if (last && releaser) {  // S(j) done: K(j) free; PV(j-1) done: V(j-1) free
+        mbar_arrive(&bars[B_KEMPTY + ((jt0 + j) & 1)]);
+        if (j > 0) mbar_arrive(&bars[B_VEMPTY + ((jt0 + j - 1) & 1)]);
+        if (j + 1 == it.n_tiles) mbar_arrive(&bars[B_QEMPTY]);
+      }
       tc_fence_after();
       // All four 32-column loads in flight, one wait.
       uint32_t sv[kBN / 32][32];
@@ -576,10 +635,11 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_PFULL + x]);
-      ++npv;
     }
     // Epilogue: wait for this tile's last PV, O / l -> bf16 -> out.
-    if (!mbar_wait(&bars[B_PVDONE + x], (npv - 1) & 1, a.status)) return;
+    if (!mbar_wait(&bars[B_PVDONE + x], nit & 1, a.status)) return;
+    ++nit;
+    if (last && releaser) mbar_arrive(&bars[B_VEMPTY + ((jt0 + it.n_tiles - 1) & 1)]);
     tc_fence_after();
     const float inv = 1.f / l;
     uint16_t* orow = a.out + (int64_t)(it.q_row0 + x * a.tok_per_tile + tok) * a.out_stride +
@@ -622,7 +682,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Lay::kNumBars);
   Sched* sc = reinterpret_cast<Sched*>(smem + Lay::kSched);
   const int warp = threadIdx.x >> 5;
-  if (warp == kProducerWarp && a.use_list) build_schedule(a, sc);
+  if (warp == kProducerWarp) build_schedule(a, sc);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_QFULL], 1);
@@ -636,6 +696,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
       mbar_init(&bars[B_PFULL + i], 4);
       mbar_init(&bars[B_PVDONE + i], 1);
       mbar_init(&bars[B_OFREE + i], 4);
+      mbar_init(&bars[B_VREADY + i], 1);
     }
     mbar_init(&bars[B_DRAIN], 1);
     fence_mbar_init();
@@ -653,8 +714,10 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
     if (warp == kProducerWarp)
       producer_role<D>(a, &tmQ, &tmK, &tmV, smem, bars, sc);
-    else if (warp == kMmaWarp)
+    else if (warp == kMmaWarp && (threadIdx.x & 31) == 0)
       mma_role<D>(a, smem, bars, tbase, sc);
+    else if (warp == kVFixWarp)
+      vfix_role<D>(a, smem, bars, sc);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     softmax_role<D>(a, smem, bars, tbase, sc);
@@ -777,7 +840,8 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
     return KVP_ERR_UNSUPPORTED;
   }
   const int grid = (int)(items < num_sms ? items : num_sms);
-  a.use_list = items <= (long long)128 * grid ? 1 : 0;
+  a.use_list = items <= (long long)kMaxListItems * grid ? 1 : 0;
+  a.cu_in_smem = num_seqs + 1 <= kCuCap ? 1 : 0;
   cudaError_t e = head_dim == 128 ? launch_t<128>(mq, mk, mv, a, grid, stream)
                                   : launch_t<64>(mq, mk, mv, a, grid, stream);
   if (e != cudaSuccess) {
