@@ -98,6 +98,7 @@ struct Item {
 constexpr int kCostBins = 256;
 constexpr int kMaxListItems = 128;
 constexpr int kCuCap = 520;  // cu_seqlens entries cached in shared memory (num_seqs + 1)
+constexpr int kMaxPairs = 8192;  // (pair rank, sequence) entries the cost-sorted deal handles
 
 // Per-CTA schedule state in shared memory (written before the roles start).
 struct Sched {
@@ -107,6 +108,7 @@ struct Sched {
   int items[kMaxListItems];   // item indices dealt to this CTA
   Item list[kMaxListItems];   // the same items, decoded
   int cu[2][kCuCap];          // cu_seqlens_q, cu_seqlens_k
+  uint8_t cost[kMaxPairs];    // cost bin of each (rank, sequence) pair, 0 = no work
 };
 constexpr uint32_t kSchedBytes = (sizeof(Sched) + 15) & ~15u;
 
@@ -127,6 +129,7 @@ struct Layout {
   // kernel checks it and reports KVP_ERR_DEVICE_DATA otherwise).
   static constexpr uint32_t kAlloc = kTotal + 128;
 };
+static_assert(Layout<128>::kAlloc <= 227 * 1024, "shared memory per CTA");
 
 // Barrier indices.
 enum : int {
@@ -213,29 +216,40 @@ __device__ __forceinline__ bool pair_cost(const PrefillArgs& a, const Cu& cu, in
   return true;
 }
 
-// Built by one warp before the roles start: cu_seqlens into shared memory,
-// the cost-sorted deal, then the dealt items decoded.
-__device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
-  const int lane = threadIdx.x & 31;
-  if (a.cu_in_smem) {
-    for (int i = lane; i <= a.num_seqs; i += 32) {
+// First part of the schedule, run by every thread of the CTA: cu_seqlens into
+// shared memory, each pair's cost bin, and the per-bin item counts.
+__device__ void schedule_costs(const PrefillArgs& a, Sched* sc) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  if (a.cu_in_smem)
+    for (int i = tid; i <= a.num_seqs; i += nt) {
       sc->cu[0][i] = a.cu_q[i];
       sc->cu[1][i] = a.cu_k[i];
     }
-    __syncwarp();
-  }
+  if (a.use_list)
+    for (int i = tid; i < kCostBins; i += nt) sc->bins[i] = 0;
+  __syncthreads();
   if (!a.use_list) return;
   const Cu cu = cu_view(a, sc);
-  const int H = a.num_kv_heads, P = gridDim.x;
   const int npi = a.max_pairs * a.num_seqs;
-  for (int i = lane; i < kCostBins; i += 32) sc->bins[i] = 0;
-  if (lane == 0) sc->count = 0;
-  __syncwarp();
-  for (int idx = lane; idx < npi; idx += 32) {
+  for (int idx = tid; idx < npi; idx += nt) {
     int v;
-    if (pair_cost(a, cu, idx, v)) atomicAdd(&sc->bins[v], (uint32_t)H);
+    const bool ok = pair_cost(a, cu, idx, v);
+    sc->cost[idx] = ok ? (uint8_t)v : (uint8_t)0;
+    if (ok) atomicAdd(&sc->bins[v], (uint32_t)a.num_kv_heads);
   }
-  __syncwarp();
+  __syncthreads();
+}
+
+// Second part, one warp: positions in the cost-sorted order and this CTA's
+// share of the snake deal, then the dealt items decoded.  Position p goes to
+// CTA p mod 2P when that is < P, else to 2P - 1 - (p mod 2P); so this CTA's
+// k-th item sits at position (k / 2) * 2P + (k even ? bx : 2P - 1 - bx), and
+// the list comes out in position order (heaviest first) without sorting.
+__device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
+  const int lane = threadIdx.x & 31;
+  const Cu cu = cu_view(a, sc);
+  const uint32_t H = a.num_kv_heads, P2 = 2 * gridDim.x, bx = blockIdx.x;
+  const int npi = a.max_pairs * a.num_seqs;
   // Exclusive prefix in descending cost: lane 0 owns the 8 highest bins.
   const int base = (31 - lane) * 8;
   uint32_t sum = 0;
@@ -247,6 +261,7 @@ __device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
     const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
+  const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
   uint32_t run = incl - sum;
   __syncwarp();
 #pragma unroll
@@ -259,8 +274,8 @@ __device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
   // Positions in (rank, sequence) order; equal costs keep index order.
   for (int b0 = 0; b0 < npi; b0 += 32) {
     const int idx = b0 + lane;
-    int v = -1;
-    const bool ok = idx < npi && pair_cost(a, cu, idx, v);
+    const int v = idx < npi ? sc->cost[idx] : 0;
+    const bool ok = v != 0;
     const unsigned same = __match_any_sync(0xffffffffu, ok ? v : -1);
     const unsigned lower = same & ((1u << lane) - 1u);
     uint32_t pos0 = 0;
@@ -268,19 +283,21 @@ __device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
     __syncwarp();
     if (ok && lower == 0) sc->bins[v] += (uint32_t)__popc(same) * H;
     if (ok) {
-      for (int g = 0; g < H; ++g) {
-        const uint32_t p = pos0 + g;
-        const int round = p / P, j = p - round * P;
-        const int cta = (round & 1) ? P - 1 - j : j;
-        if (cta == (int)blockIdx.x) {
-          const int slot = atomicAdd(&sc->count, 1);
-          if (slot < kMaxListItems) sc->items[slot] = idx * H + g;
-        }
+      const uint32_t per = pos0 / P2;
+      for (uint32_t q = per;; ++q) {
+        const uint32_t c0 = q * P2 + bx, c1 = q * P2 + (P2 - 1 - bx);
+        if (c0 >= pos0 + H) break;
+        if (c0 >= pos0 && 2 * q < (uint32_t)kMaxListItems)
+          sc->items[2 * q] = idx * (int)H + (int)(c0 - pos0);
+        if (c1 >= pos0 && c1 < pos0 + H && 2 * q + 1 < (uint32_t)kMaxListItems)
+          sc->items[2 * q + 1] = idx * (int)H + (int)(c1 - pos0);
       }
     }
     __syncwarp();
   }
-  const int n = min(sc->count, kMaxListItems);
+  const uint32_t rem = total % P2;
+  const int n = min((int)(2 * (total / P2) + (rem > bx) + (rem > P2 - 1 - bx)), kMaxListItems);
+  if (lane == 0) sc->count = n;
   for (int i = lane; i < n; i += 32) decode_item(a, cu, sc->items[i], sc->list[i]);
   __syncwarp();
 }
@@ -682,7 +699,8 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Lay::kNumBars);
   Sched* sc = reinterpret_cast<Sched*>(smem + Lay::kSched);
   const int warp = threadIdx.x >> 5;
-  if (warp == kProducerWarp) build_schedule(a, sc);
+  schedule_costs(a, sc);
+  if (warp == kProducerWarp && a.use_list) build_schedule(a, sc);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_QFULL], 1);
@@ -840,7 +858,10 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
     return KVP_ERR_UNSUPPORTED;
   }
   const int grid = (int)(items < num_sms ? items : num_sms);
-  a.use_list = items <= (long long)kMaxListItems * grid ? 1 : 0;
+  a.use_list = items <= (long long)kMaxListItems * grid &&
+                       (long long)a.max_pairs * num_seqs <= kMaxPairs
+                   ? 1
+                   : 0;
   a.cu_in_smem = num_seqs + 1 <= kCuCap ? 1 : 0;
   cudaError_t e = head_dim == 128 ? launch_t<128>(mq, mk, mv, a, grid, stream)
                                   : launch_t<64>(mq, mk, mv, a, grid, stream);
