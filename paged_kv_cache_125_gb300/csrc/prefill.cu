@@ -319,6 +319,32 @@ __device__ __forceinline__ bool next_item(const PrefillArgs& a, const Sched* sc,
   return false;
 }
 
+// Transpose of a 4 x 4 matrix of 16-byte chunks held by the 4 lanes of a
+// quad: on entry lane j holds chunks 0..3 of its row in w[0..3]; on exit lane
+// j holds chunk j of rows 0..3 of the quad.  Two butterfly stages; in each, a
+// chunk moves to the partner lane when one bit of its chunk index differs
+// from the same bit of the lane index.
+__device__ __forceinline__ void quad_transpose16(uint32_t (&w)[4][4], int lane) {
+#pragma unroll
+  for (int m = 1; m <= 2; m <<= 1) {
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int k0 = 0; k0 < 4; ++k0) {
+      if (k0 & m) continue;
+      const int k1 = k0 | m;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t send = hi ? w[k0][i] : w[k1][i];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, m);
+        if (hi)
+          w[k0][i] = recv;
+        else
+          w[k1][i] = recv;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -658,29 +684,45 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
     ++nit;
     if (last && releaser) mbar_arrive(&bars[B_VEMPTY + ((jt0 + it.n_tiles - 1) & 1)]);
     tc_fence_after();
-    const float inv = 1.f / l;
-    uint16_t* orow = a.out + (int64_t)(it.q_row0 + x * a.tok_per_tile + tok) * a.out_stride +
-                     (int64_t)(it.g * a.group + h) * D;
+    uint32_t ov[D / 32][32];
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t v[32];
-      tmem_ld32(o_col + c * 32, v);
-      tmem_ld_wait();
-      if (row_valid) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint4 u;
-          u.x = pack_bf16x2(__uint_as_float(v[q * 8 + 0]) * inv, __uint_as_float(v[q * 8 + 1]) * inv);
-          u.y = pack_bf16x2(__uint_as_float(v[q * 8 + 2]) * inv, __uint_as_float(v[q * 8 + 3]) * inv);
-          u.z = pack_bf16x2(__uint_as_float(v[q * 8 + 4]) * inv, __uint_as_float(v[q * 8 + 5]) * inv);
-          u.w = pack_bf16x2(__uint_as_float(v[q * 8 + 6]) * inv, __uint_as_float(v[q * 8 + 7]) * inv);
-          *reinterpret_cast<uint4*>(orow + c * 32 + q * 8) = u;
-        }
-      }
-    }
+    for (int c = 0; c < D / 32; ++c) tmem_ld32(o_col + c * 32, ov[c]);
+    tmem_ld_wait();
+    // O is in registers: the next item's PV may overwrite it.
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(&bars[B_OFREE + x]);
+    // Stores: a lane's row is 2*D contiguous bytes, but lanes of one store
+    // instruction would each hit a different cache line.  After a 4x4
+    // transpose of 16-byte chunks within each quad of lanes, the quad writes
+    // 64 contiguous bytes of one row per instruction.
+    const float inv = 1.f / l;
+    uint16_t* orow = row_valid ? a.out +
+                                     (int64_t)(it.q_row0 + x * a.tok_per_tile + tok) * a.out_stride +
+                                     (int64_t)(it.g * a.group + h) * D
+                               : nullptr;
+    const int qb = lane & ~3, jq = lane & 3;
+    uint16_t* qrow[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      qrow[k] = reinterpret_cast<uint16_t*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(orow), qb + k));
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t w[4][4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          w[k][i] = pack_bf16x2(__uint_as_float(ov[c][8 * k + 2 * i]) * inv,
+                                __uint_as_float(ov[c][8 * k + 2 * i + 1]) * inv);
+      quad_transpose16(w, lane);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (qrow[k] != nullptr)
+          *reinterpret_cast<uint4*>(qrow[k] + c * 32 + jq * 8) =
+              make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
+    }
   }
 }
 
