@@ -44,11 +44,14 @@ N_SETS = 4
 # for the dominant kernels, with the sha256 of the kernel source they were
 # measured on; a figure whose source has changed since is reported as null.
 TRAFFIC = {
-    "decode": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu", "sha256": None, "bytes": None},
+    # decode B64 workload (one input set), one ncu --set full capture of the split kernel
+    "decode": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu",
+               "sha256": "c83d43b4f15bd4c86b53010a9cb312d104ffad5357352bf404658ab3274b97a0",
+               "bytes": 569101824 + 4088064},
     # prefill workload (8 prompts, 32/8/128), one ncu --set full capture
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
-                "sha256": "494c03c9ff99f497252379b3894f407538f2e476775e16d3395f75fbf4d31598",
-                "bytes": 121241088 + 28700672},
+                "sha256": "7f0d1f138084be63d9c0f9e978777bd8c537218863f743fc7bb58d4fc22707bc",
+                "bytes": 122565888 + 33760256},
 }
 
 
