@@ -50,7 +50,7 @@ TRAFFIC = {
                "bytes": 569101824 + 4088064},
     # prefill workload (8 prompts, 32/8/128), one ncu --set full capture
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
-                "sha256": "7f0d1f138084be63d9c0f9e978777bd8c537218863f743fc7bb58d4fc22707bc",
+                "sha256": "12dbff6aef6fea57751e9b2472606cb49331b35736521816defd51a925b687de",
                 "bytes": 122565888 + 33760256},
 }
 

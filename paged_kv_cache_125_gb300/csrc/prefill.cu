@@ -17,28 +17,30 @@
 // row sees; each K/V tile in shared memory feeds both query tiles, which
 // halves the K/V bytes moved per FLOP compared with one tile.
 //
-// Persistent CTAs (one per SM), 10 warps:
+// Persistent CTAs (one per SM), 12 warps:
 //   warp 8  TMA producer: the Q pair (one slot), K tiles (2 slots), V tiles
 //           (2 slots).  In paged mode a kv tile is loaded as block-sized
 //           sub-boxes addressed through the block table (gather folded into
 //           the loads); sub-boxes past the sequence's last key are skipped.
-//   warp 9  MMA issuer + tensor-memory owner.  TMEM columns: S_A | S_B | O_A |
-//           O_B (128 each).  Issue order per kv tile j:
-//             PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
+//   warp 9  tensor-memory owner; one of its threads issues every MMA.  TMEM
+//           columns: S_A | S_B | O_A | O_B (128 each).  Issue order per kv
+//           tile j:  PV_A(j), S_A(j+1), PV_B(j), S_B(j+1)
 //           so each softmax warpgroup computes on one tile while the tensor
-//           core works on the other tile (ping-pong).
+//           core works on the other tile (ping-pong).  PV reads P from
+//           tensor memory (the A operand of a TS-form MMA).
+//   warp 10 V fix-up: zeroes V rows past the last key before PV reads them.
 //   warps 0-3 / 4-7  softmax for tile A / B: thread r owns row r (TMEM lane
 //           r).  Reads S with tcgen05.ld, masks only where a tile crosses the
 //           diagonal, keeps a running max per row and rescales O only when
 //           the max grows by more than 2^8 (exact: O and the row sum share the
-//           stale reference), writes P as bf16 into shared memory in the
-//           128-byte-swizzled K-major layout the MMA reads, and at the end of
-//           an item normalises O and stores bf16.
+//           stale reference), writes P as bf16 pairs over the first 64
+//           columns of its S region, and at the end of an item normalises O
+//           and stores bf16.  The warpgroup of an item's last tile releases
+//           the K, V and Q slots once it sees the S that last read them.
 // Synchronisation facts the design relies on: a tcgen05.commit arrives only
 // when every earlier MMA of the issuing thread has completed, so the commit
-// after S_X(j) also says PV_X(j-1) is done (O_X may be rescaled).  The single
-// P buffer alternates between the tiles in MMA order; before writing P each
-// warpgroup waits for the PV that read P last.
+// after S_X(j+1) also says PV_X(j) is done (O_X may be rescaled, and P_X's
+// columns, which S_X(j+1) overwrites, have been read).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -51,10 +53,10 @@ namespace {
 constexpr int kBM = 128;  // query rows per tile
 constexpr int kBN = 128;  // keys per kv tile
 // Three warpgroups: softmax A (warps 0-3), softmax B (4-7), and a control
-// group (warp 8 TMA producer, warp 9 MMA issuer, warps 10-11 idle).  The
-// launch gives every thread 168 registers (384 x 168 = 64512); the control
-// group hands registers back with setmaxnreg and the softmax groups take them:
-// 128 x (200 + 200 + 104) = 64512, the launch's total.
+// group (warp 8 TMA producer, warp 9 MMA issuer, warp 10 V fix-up, warp 11
+// idle).  The launch gives every thread 168 registers (384 x 168 = 64512);
+// the control group hands registers back with setmaxnreg and the softmax
+// groups take them: 128 x (200 + 200 + 104) = 64512, the launch's total.
 constexpr int kThreadsPF = 384;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
