@@ -65,6 +65,7 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
+    p.add_argument("--no-copy-blocks", action="store_true")
     p.add_argument("--only", choices=["decode", "prefill"], default=None,
                    help="run one half only (profiling); the JSON line then carries that half")
     p.add_argument("--sets", type=int, default=N_SETS, help="input sets in rotation")
@@ -448,6 +449,52 @@ def measure_prefill(args, kvp, W, dev, stream, world, peaks):
                                   "ms_per_launch": round(ms_prefill, 5)}}}
 
 
+def measure_copy_blocks(args, kvp, dev, stream, world, peaks):
+    """Copy-on-write block copies (page 3, "场景优化1：Parallel Memory Shared"):
+    one call copies 64 (src, dst) block pairs in all 56 planes of a 28-layer
+    cache of 512 KiB blocks (Qwen3-0.6B shape, bs 256) = 3.76 GB of traffic;
+    every byte read once and written once."""
+    import torch
+    layers, nb, bs, hkv, d, pairs = 28, 160, 256, 8, 128, 64
+    cache = torch.zeros((2, layers, nb, bs, hkv, d), dtype=torch.bfloat16, device=dev)
+    g = torch.Generator().manual_seed(2)
+    perm = torch.randperm(nb, generator=g)
+    dst = perm[:pairs]
+    src = perm[pairs:][torch.randint(0, nb - pairs, (pairs,), generator=g)]
+    mapping = torch.stack([src, dst], dim=1).to(torch.int32).to(dev)
+    block_bytes = bs * hkv * d * 2
+    step_bytes = 2 * pairs * 2 * layers * block_bytes
+    steps = max(10, min(50, args.steps // 100))
+    for _ in range(3):
+        kvp.kv_copy_blocks(cache, mapping)
+    torch.cuda.synchronize()
+    barrier(world)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    w0 = time.perf_counter()
+    for a, b in evs:
+        a.record()
+        kvp.kv_copy_blocks(cache, mapping)
+        b.record()
+    torch.cuda.synchronize()
+    w1 = time.perf_counter()
+    barrier(world)
+    assert kvp.device_status() == 0, "device status after the copy loop"
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    bps, ms = aggregate(step_bytes, ms, world)
+    achieved = step_bytes / (ms * 1e-3) / 1e9
+    del cache
+    return {"window": (w0, w1),
+            "line": {"workload": f"copy-on-write: {pairs} block pairs x {2 * layers} planes "
+                                 f"(28 layers K+V, bs {bs}, 8x128, 512 KiB blocks), pool {nb} blocks",
+                     "value": round(bps / 1e9, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
+                     "steps": steps,
+                     "roofline": {"kernel": "kv_copy_blocks", "bound": "hbm", "achieved": round(achieved, 1),
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                                  "algorithmic_bytes": step_bytes, "peak_source": peaks["source"],
+                                  "ms_per_launch": round(ms, 5)}}}
+
+
 def run_ours(args, rank, world, local):
     import torch
     import paged_kv_cache_125_gb300 as kvp
@@ -471,6 +518,10 @@ def run_ours(args, rank, world, local):
     if args.only != "decode" and not args.no_prefill:
         pre = measure_prefill(args, kvp, W, dev, stream, world, peaks)
         windows.append(pre["window"])
+    cb = None
+    if args.only is None and not args.no_copy_blocks:
+        cb = measure_copy_blocks(args, kvp, dev, stream, world, peaks)
+        windows.append(cb["window"])
     time.sleep(0.1)
     clocks = sampler.stop(windows)
 
@@ -495,14 +546,18 @@ def run_ours(args, rank, world, local):
                        "l2": f"{args.sets} input sets in rotation ({dec['footprint_gb']:.1f} GB of pools) vs 126 MB L2",
                        "graph": "each step is two CUDA graph replays (store, attention)"},
             "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
-            "gpu_launches": 3 * args.steps + (0 if pre is None else 2 * pre["line"]["steps"]),
+            "gpu_launches": 3 * args.steps + (0 if pre is None else 2 * pre["line"]["steps"])
+                            + (0 if cb is None else cb["line"]["steps"]),
             "gpu_launches_by_region": {"decode": {"kv_store": args.steps, "decode_split": args.steps,
                                                   "decode_merge": args.steps},
                                        "prefill": None if pre is None else
                                        {"kv_store": pre["line"]["steps"],
-                                        "prefill": pre["line"]["steps"]}},
+                                        "prefill": pre["line"]["steps"]},
+                                       "copy_blocks": None if cb is None else
+                                       {"kv_copy_blocks": cb["line"]["steps"]}},
             "clocks": clocks,
-            "prefill": None if pre is None else pre["line"]}
+            "prefill": None if pre is None else pre["line"],
+            "copy_blocks": None if cb is None else cb["line"]}
     print(json.dumps(line), flush=True)
 
 

@@ -102,6 +102,39 @@ int kv_store(const kvp_bf16 *k, const kvp_bf16 *v, int64_t k_stride_tok, int64_t
              int head_dim, kvp_stream_t stream);
 
 /*
+ * kv_copy_blocks - copy-on-write copies of whole cache blocks.
+ *
+ * For every pair i < num_pairs with src = block_mapping[2i] and
+ * dst = block_mapping[2i+1], and every plane p < num_planes:
+ *     cache[p * plane_stride + dst * block_elems + e] =
+ *         cache[p * plane_stride + src * block_elems + e],   e < block_elems
+ * bit-exactly.  A plane is one layer's K or one layer's V cache: the engine's
+ * [2, layers, num_blocks, block_size, num_kv_heads, head_dim] tensor is
+ * num_planes = 2 * layers planes with plane_stride = num_blocks * block_elems
+ * and block_elems = block_size * num_kv_heads * head_dim.
+ * Source: "【nano-vllm 学习】04 - 自顶向下的引擎调度层源码学习2", section
+ * "场景优化1：Parallel Memory Shared": when a sequence must append into a
+ * block it shares with others (reference count > 1), the engine gives it a
+ * new physical block holding a copy of the shared one (copy on write).
+ *
+ *   cache          bf16 base of plane 0 (device)
+ *   num_planes     >= 1
+ *   plane_stride   elements from one plane to the next (>= num_blocks*block_elems)
+ *   num_blocks     blocks per plane
+ *   block_elems    elements per block
+ *   block_mapping  [num_pairs, 2] int32 (src, dst), device
+ * Destinations must be distinct, and no destination may be the source of
+ * another pair (the engine copies into freshly allocated blocks); otherwise
+ * the result is undefined.  num_pairs == 0 is a no-op.  A src or dst outside
+ * [0, num_blocks) skips that pair and sets KVP_ERR_DEVICE_DATA.  The 16-byte
+ * path is taken when cache, plane_stride and block_elems are 16-byte / 8-element
+ * aligned; other layouts are copied element by element.
+ */
+int kv_copy_blocks(kvp_bf16 *cache, int64_t num_planes, int64_t plane_stride, int64_t num_blocks,
+                   int64_t block_elems, const int32_t *block_mapping, int64_t num_pairs,
+                   kvp_stream_t stream);
+
+/*
  * attn_prefill_varlen - causal attention over sequences packed back to back.
  *
  * Sequence b owns query rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1 and has

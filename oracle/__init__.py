@@ -47,11 +47,12 @@ def _load():
             i64, i32, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_double
             lib.oracle_kv_store.argtypes = [p, p, i64, i64, p, i64, p, p, i64, i32, i32, i32]
             lib.oracle_gather.argtypes = [p, i64, i32, i32, i32, p, i32, i64, p]
+            lib.oracle_copy_blocks.argtypes = [p, i64, i64, i64, i64, p, i64]
             lib.oracle_prefill.argtypes = [p, i64, p, p, i64, p, p, i64, i32, p, i32, p, p,
                                            i32, i32, i32, i32, dbl, p, i64, p]
             lib.oracle_decode.argtypes = [p, i64, p, p, i64, i32, p, i32, p, i32, i32, i32,
                                           i32, dbl, p, i32, p]
-            for f in (lib.oracle_kv_store, lib.oracle_gather, lib.oracle_prefill,
+            for f in (lib.oracle_kv_store, lib.oracle_gather, lib.oracle_copy_blocks, lib.oracle_prefill,
                       lib.oracle_decode, lib.oracle_num_threads):
                 f.restype = ctypes.c_int
             _lib = lib
@@ -117,6 +118,19 @@ def gather(cache: np.ndarray, block_table_row, num_tokens: int) -> np.ndarray:
     _check(lib.oracle_gather(_ptr(np.ascontiguousarray(cache)), nb, bs, hkv, d, _ptr(bt),
                              bt.shape[0], num_tokens, _ptr(out)), "gather")
     return out
+
+
+def copy_blocks(kv_cache: np.ndarray, block_mapping) -> None:
+    """Copy on write in place: kv_cache is uint16 [..., NB, bs, Hkv, d] (every
+    leading index is one plane); block_mapping is [n, 2] (src, dst)."""
+    lib = _load()
+    assert kv_cache.dtype == np.uint16 and kv_cache.flags.c_contiguous
+    nb = kv_cache.shape[-4]
+    be = int(np.prod(kv_cache.shape[-3:]))
+    planes = kv_cache.size // (nb * be)
+    bm = _arr(block_mapping, np.int32).reshape(-1, 2)
+    _check(lib.oracle_copy_blocks(_ptr(kv_cache), planes, nb * be, nb, be, _ptr(bm), bm.shape[0]),
+           "copy_blocks")
 
 
 def prefill(q, cu_seqlens_q, cu_seqlens_k, num_heads: int, num_kv_heads: int, scale: float,

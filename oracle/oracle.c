@@ -16,7 +16,9 @@
  *        block_tables, context_lens, slot_mapping).
  *   [P3] "【nano-vllm 学习】04 - 自顶向下的引擎调度层源码学习2", section
  *        "KV-Cache … 是什么？": Attention(Q,K,V) = softmax(QK^T / sqrt(d_k)) V with
- *        a causal mask (masked scores -> -inf -> weight 0), and S_i = { j <= i }.
+ *        a causal mask (masked scores -> -inf -> weight 0), and S_i = { j <= i };
+ *        section "场景优化1：Parallel Memory Shared": copy on write of a shared
+ *        block into a freshly allocated one.
  *
  * Readings where the pages leave a step open (each is also listed in the design
  * notes):
@@ -104,6 +106,27 @@ int oracle_gather(const uint16_t *cache, int64_t num_blocks, int block_size,
       for (int e = 0; e < head_dim; ++e)
         out[(p * num_kv_heads + h) * head_dim + e] =
             cache[((blk * block_size + off) * num_kv_heads + h) * head_dim + e];
+  }
+  return ORACLE_OK;
+}
+
+/*
+ * Copy on write [P3 "场景优化1：Parallel Memory Shared": a sequence that must
+ * append into a block shared with others gets a new physical block holding a
+ * copy of the shared one].  For every pair i (src = mapping[2i],
+ * dst = mapping[2i+1]) and every plane p (one layer's K or V cache), copy the
+ * block_elems bf16 bits of block src to block dst.  Pairs are applied in order.
+ */
+int oracle_copy_blocks(uint16_t *cache, int64_t num_planes, int64_t plane_stride,
+                       int64_t num_blocks, int64_t block_elems, const int32_t *mapping,
+                       int64_t num_pairs) {
+  for (int64_t i = 0; i < num_pairs; ++i) {
+    int64_t src = mapping[2 * i], dst = mapping[2 * i + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) return ORACLE_BAD_BLOCK;
+    for (int64_t p = 0; p < num_planes; ++p)
+      for (int64_t e = 0; e < block_elems; ++e)
+        cache[p * plane_stride + dst * block_elems + e] =
+            cache[p * plane_stride + src * block_elems + e];
   }
   return ORACLE_OK;
 }

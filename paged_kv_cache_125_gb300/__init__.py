@@ -8,6 +8,7 @@ library; all the work runs in the library's CUDA kernels.  There is no CPU or
 PyTorch fallback: if the library cannot be loaded, every call raises.
 
     kv_store(k, v, slot_mapping, k_cache, v_cache)
+    kv_copy_blocks(kv_cache, block_mapping)
     attn_prefill_varlen(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, ...)
     attn_decode_paged(q, k_cache, v_cache, block_tables, context_lens, max_context_len, ...)
 """
@@ -18,7 +19,7 @@ import math
 import os
 import threading
 
-__all__ = ["kv_store", "attn_prefill_varlen", "attn_decode_paged", "attn_decode_workspace_size",
+__all__ = ["kv_store", "kv_copy_blocks", "attn_prefill_varlen", "attn_decode_paged", "attn_decode_workspace_size",
            "attn_decode_paged_noalloc",
            "device_status", "library", "library_path", "KvpError"]
 
@@ -36,6 +37,7 @@ SIGNATURES = {
     "kvp_version": (_I32, []),
     "kvp_device_status": (_I32, []),
     "kv_store": (_I32, [_P, _P, _I64, _I64, _P, _I64, _P, _P, _I64, _I32, _I32, _I32, _P]),
+    "kv_copy_blocks": (_I32, [_P, _I64, _I64, _I64, _I64, _P, _I64, _P]),
     "attn_prefill_varlen": (_I32, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _I64, _I32, _P, _I32,
                                    _P, _P, _I32, _I32, _I32, _P, _I32, _I32, _I32, _F32, _P, _I64,
                                    _P]),
@@ -140,6 +142,28 @@ def kv_store(k, v, slot_mapping, k_cache, v_cache) -> None:
     ks, vs = _rows(k, "k", hkv, d), _rows(v, "v", hkv, d)
     _check(library().kv_store(_ptr(k), _ptr(v), ks, vs, _ptr(slot_mapping), n, _ptr(k_cache),
                               _ptr(v_cache), nb, bs, hkv, d, _stream(k_cache)))
+
+
+def kv_copy_blocks(kv_cache, block_mapping) -> None:
+    """Copy-on-write block copies in every plane of ``kv_cache``.
+
+    ``kv_cache`` is the engine's cache tensor ``[..., num_blocks, block_size,
+    num_kv_heads, head_dim]`` (bf16, contiguous; every leading index, e.g. k/v
+    and layer, is one plane).  ``block_mapping`` is ``[n, 2]`` int32 (src, dst)
+    on the same device."""
+    import torch
+    if kv_cache.dtype != torch.bfloat16 or not kv_cache.is_cuda or not kv_cache.is_contiguous():
+        raise ValueError("kv_cache must be a contiguous bf16 CUDA tensor")
+    if kv_cache.dim() < 4:
+        raise ValueError("kv_cache must be [..., num_blocks, block_size, num_kv_heads, head_dim]")
+    _require(block_mapping, "block_mapping", torch.int32, 2, kv_cache.device)
+    if block_mapping.shape[1] != 2 or not block_mapping.is_contiguous():
+        raise ValueError("block_mapping must be a contiguous [n, 2] tensor")
+    nb = kv_cache.shape[-4]
+    block_elems = kv_cache.shape[-3] * kv_cache.shape[-2] * kv_cache.shape[-1]
+    planes = kv_cache.numel() // (nb * block_elems)
+    _check(library().kv_copy_blocks(_ptr(kv_cache), planes, nb * block_elems, nb, block_elems,
+                                    _ptr(block_mapping), block_mapping.shape[0], _stream(kv_cache)))
 
 
 def attn_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len, block_size) -> int:

@@ -119,6 +119,27 @@ int kv_store(const kvp_bf16* k, const kvp_bf16* v, int64_t k_stride_tok, int64_t
   return KVP_OK;
 }
 
+int kv_copy_blocks(kvp_bf16* cache, int64_t num_planes, int64_t plane_stride, int64_t num_blocks,
+                   int64_t block_elems, const int32_t* block_mapping, int64_t num_pairs,
+                   kvp_stream_t stream) {
+  if (num_pairs < 0) return fail(KVP_ERR_INVALID_ARG, "kv_copy_blocks: num_pairs < 0");
+  if (num_planes <= 0 || num_blocks <= 0 || block_elems <= 0)
+    return fail(KVP_ERR_INVALID_ARG, "kv_copy_blocks: non-positive shape");
+  if (plane_stride < num_blocks * block_elems)
+    return fail(KVP_ERR_INVALID_ARG, "kv_copy_blocks: plane_stride < num_blocks * block_elems");
+  if (num_pairs == 0) return KVP_OK;
+  if (!cache || !block_mapping) return fail(KVP_ERR_INVALID_ARG, "kv_copy_blocks: null pointer");
+  int dev, *status, sms;
+  int rc = device_info(&dev, &status, &sms);
+  if (rc) return rc;
+  const bool vec16 = aligned16(cache) && plane_stride % 8 == 0 && block_elems % 8 == 0;
+  cudaError_t e = kvp::launch_copy_blocks(cache, num_planes, plane_stride, num_blocks, block_elems,
+                                          block_mapping, num_pairs, vec16, sms, status,
+                                          (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "kv_copy_blocks launch");
+  return KVP_OK;
+}
+
 size_t attn_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len,
                                   int block_size) {
   (void)block_size;

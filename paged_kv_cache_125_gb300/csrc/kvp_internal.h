@@ -19,6 +19,12 @@ cudaError_t launch_kv_store(const uint16_t* k, const uint16_t* v, int64_t k_stri
                             uint16_t* v_cache, int64_t total_slots, int row_elems, bool vec16,
                             int num_sms, int* status, cudaStream_t stream);
 
+// copy_blocks.cu
+cudaError_t launch_copy_blocks(uint16_t* cache, int64_t num_planes, int64_t plane_stride,
+                               int64_t num_blocks, int64_t block_elems, const int32_t* mapping,
+                               int64_t num_pairs, bool vec16, int num_sms, int* status,
+                               cudaStream_t stream);
+
 // decode.cu
 struct DecodePlan {
   int ctas;            // persistent CTAs of the split kernel (one per SM at most)

@@ -9,7 +9,10 @@
   nothing (paging, page 3 "PageAttention"); a prefix-cached suffix prefill
   equals the same rows of a full prefill, and decoding token L-1 equals row L-1
   of a causal prefill (causal invariance, page 3 "KV-Cache … 是什么？");
-* store-then-gather returns the stored bits, and the pages' paging examples.
+* store-then-gather returns the stored bits, and the pages' paging examples;
+* copy on write (page 3, "场景优化1：Parallel Memory Shared"): two sampled
+  sequences share a partly filled prompt block; after the copy each appends
+  its own token and reads back exactly prompt + own token, in every layer.
 """
 import json
 import os
@@ -304,3 +307,66 @@ def test_decode_subset_matches_full():
     full = oracle.decode(q, c["kc"], c["vc"], c["bt"], ctx, 4, 2, 0.125)
     sub = oracle.decode(q, c["kc"], c["vc"], c["bt"], ctx, 4, 2, 0.125, seqs=[2, 0])
     assert np.array_equal(sub[[0, 2]], full[[0, 2]]) and np.all(sub[1] == 0)
+
+
+def test_copy_on_write_parallel_sampling():
+    """Page 3's parallel-sampling example: sequences A1 and A2 come from one
+    prompt and share its physical blocks; the last one is partly filled.  A1
+    must append, sees a reference count of 2, gets a new block holding a copy
+    of the shared one, and writes its token there; A2 then appends into the
+    original block.  Checked in each of 3 layers (6 planes) through the
+    store and gather of the pages' slot formula: each sequence reads back
+    exactly the prompt rows followed by its own new row."""
+    g = torch.Generator().manual_seed(21)
+    layers, nb, bs, hkv, d = 3, 12, 4, 2, 8
+    prompt_len = 6                      # blocks: one full, one with 2 of 4 slots
+    table = [7, 2]                      # shared physical blocks of the prompt
+    cache = np.full((2, layers, nb, bs, hkv, d), 0x7FC0, dtype=np.uint16)
+    prompt = torch.randn((2, layers, prompt_len, hkv, d), generator=g).to(torch.bfloat16)
+    slots = torch.tensor(W.slots_of_positions(table, range(prompt_len), bs), dtype=torch.int32)
+    for layer in range(layers):
+        kc, vc = cache[0, layer], cache[1, layer]
+        oracle.kv_store(prompt[0, layer], prompt[1, layer], slots, kc, vc)
+    new_block = 9                       # free block given to A1
+    oracle.copy_blocks(cache, [[table[-1], new_block]])
+    t1 = [table[0], new_block]
+    t2 = list(table)
+    tok = torch.randn((2, 2, layers, 1, hkv, d), generator=g).to(torch.bfloat16)  # [seq, k/v, layer]
+    pos = prompt_len                    # the appended token's position
+    for layer in range(layers):
+        for seq, bt in ((0, t1), (1, t2)):
+            s_ = torch.tensor(W.slots_of_positions(bt, [pos], bs), dtype=torch.int32)
+            oracle.kv_store(tok[seq, 0, layer], tok[seq, 1, layer], s_, cache[0, layer], cache[1, layer])
+    u = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    for layer in range(layers):
+        for kv in range(2):
+            for seq, bt in ((0, t1), (1, t2)):
+                got = oracle.gather(cache[kv, layer], bt, prompt_len + 1)
+                want = np.concatenate([u(prompt[kv, layer]), u(tok[seq, kv, layer])])
+                assert np.array_equal(got, want), (layer, kv, seq)
+    # blocks nobody wrote keep the poison
+    untouched = [b for b in range(nb) if b not in (7, 2, 9)]
+    assert np.all(cache[:, :, untouched] == 0x7FC0)
+
+
+def test_copy_blocks_leaves_everything_but_destinations():
+    """Several pairs over 4 planes: every destination block equals its
+    source's previous content; every other block (sources included) keeps
+    its bits."""
+    rng = np.random.default_rng(5)
+    cache = rng.integers(0, 1 << 16, size=(4, 20, 3, 2, 8), dtype=np.uint16)
+    before = cache.copy()
+    pairs = [[3, 11], [3, 12], [0, 19], [7, 5]]
+    oracle.copy_blocks(cache, pairs)
+    dsts = {d_ for _, d_ in pairs}
+    for s_, d_ in pairs:
+        assert np.array_equal(cache[:, d_], before[:, s_])
+    for b in range(20):
+        if b not in dsts:
+            assert np.array_equal(cache[:, b], before[:, b])
+
+
+def test_copy_blocks_rejects_out_of_range():
+    cache = np.zeros((2, 4, 2, 1, 8), dtype=np.uint16)
+    with pytest.raises(oracle.OracleError):
+        oracle.copy_blocks(cache, [[0, 4]])
