@@ -449,6 +449,52 @@ def measure_prefill(args, kvp, W, dev, stream, world, peaks):
                                   "ms_per_launch": round(ms_prefill, 5)}}}
 
 
+def measure_mixed(args, kvp, W, dev, stream, world, peaks):
+    """One engine step mixing chunked prefill and decode in a single varlen
+    paged prefill call (4 prompt chunks, 3772 tokens, + 128 decode rows,
+    32/8/128): store of the new rows + the attention call, CUDA graphs over
+    2 input sets in rotation."""
+    wm = W.mixed_step_workload()
+    flops = prefill_flops(wm)
+    m = wm.steps[0].attn.meta
+    # algorithmic bytes: K and V of every sequence's keys once per kv head, q read, out written
+    kv_bytes = int(m.cu_seqlens_k[-1]) * wm.num_kv_heads * wm.head_dim * 2 * 2
+    qo_bytes = int(m.cu_seqlens_q[-1]) * wm.num_heads * wm.head_dim * 2 * 2
+    nbytes = kv_bytes + qo_bytes
+    msets = [DeviceSet(wm, dev) for _ in range(2)]
+    mstore = capture(lambda s: store_call(kvp, s), msets, stream)
+    mattn = capture(lambda s: prefill_call(kvp, s, wm), msets, stream)
+    steps = max(50, min(400, args.steps // 10))
+    ms_step, ms_call, win = timed_loop(mstore, mattn, steps, args.warmup, world)
+    assert kvp.device_status() == 0, "device status after the mixed loop"
+    fps, ms_step = aggregate(flops, ms_step, world)
+    tf_call = flops / (ms_call * 1e-3) / 1e12
+    gbs_call = nbytes / (ms_call * 1e-3) / 1e9
+    # the binding roofline is the larger of the two lower bounds on the call's time
+    hbm_bound = nbytes / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12)
+    del mstore, mattn, msets
+    return {"window": win, "steps": steps,
+            "line": {"workload": wm.description, "value": round(fps / 1e12, 2), "unit": "TFLOP/s",
+                     "ms_per_step": round(ms_step, 4), "steps": steps,
+                     "step": "kv_store of all new rows + attn_prefill_varlen over chunks and decode rows",
+                     "roofline": ({"kernel": "attn_prefill_varlen (mixed)", "bound": "hbm",
+                                   "achieved": round(gbs_call, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                   "frac": round(gbs_call / peaks["hbm_gbs"], 4), "traffic": None,
+                                   "algorithmic_bytes": nbytes, "peak_source": peaks["source"],
+                                   "ms_per_launch": round(ms_call, 5),
+                                   "tensor": {"achieved_tflops": round(tf_call, 1),
+                                              "frac_of_bf16_burst": round(tf_call / peaks["bf16_tflops"], 4),
+                                              "algorithmic_flops": flops}}
+                                  if hbm_bound else
+                                  {"kernel": "attn_prefill_varlen (mixed)", "bound": "tensor",
+                                   "achieved": round(tf_call, 1), "peak": peaks["bf16_tflops"],
+                                   "unit": "TFLOP/s", "frac": round(tf_call / peaks["bf16_tflops"], 4),
+                                   "traffic": None, "algorithmic_flops": flops,
+                                   "peak_source": peaks["source"] + " bf16 burst",
+                                   "ms_per_launch": round(ms_call, 5),
+                                   "hbm": {"achieved_gbs": round(gbs_call, 1), "algorithmic_bytes": nbytes}})}}
+
+
 def measure_copy_blocks(args, kvp, dev, stream, world, peaks):
     """Copy-on-write block copies (page 3, "场景优化1：Parallel Memory Shared"):
     one call copies 64 (src, dst) block pairs in all 56 planes of a 28-layer
@@ -518,6 +564,10 @@ def run_ours(args, rank, world, local):
     if args.only != "decode" and not args.no_prefill:
         pre = measure_prefill(args, kvp, W, dev, stream, world, peaks)
         windows.append(pre["window"])
+    mx = None
+    if args.only is None and not args.no_prefill:
+        mx = measure_mixed(args, kvp, W, dev, stream, world, peaks)
+        windows.append(mx["window"])
     cb = None
     if args.only is None and not args.no_copy_blocks:
         cb = measure_copy_blocks(args, kvp, dev, stream, world, peaks)
@@ -547,16 +597,20 @@ def run_ours(args, rank, world, local):
                        "graph": "each step is two CUDA graph replays (store, attention)"},
             "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
             "gpu_launches": 3 * args.steps + (0 if pre is None else 2 * pre["line"]["steps"])
-                            + (0 if cb is None else cb["line"]["steps"]),
+                            + (0 if cb is None else cb["line"]["steps"])
+                            + (0 if mx is None else 2 * mx["steps"]),
             "gpu_launches_by_region": {"decode": {"kv_store": args.steps, "decode_split": args.steps,
                                                   "decode_merge": args.steps},
                                        "prefill": None if pre is None else
                                        {"kv_store": pre["line"]["steps"],
                                         "prefill": pre["line"]["steps"]},
                                        "copy_blocks": None if cb is None else
-                                       {"kv_copy_blocks": cb["line"]["steps"]}},
+                                       {"kv_copy_blocks": cb["line"]["steps"]},
+                                       "mixed": None if mx is None else
+                                       {"kv_store": mx["steps"], "prefill": mx["steps"]}},
             "clocks": clocks,
             "prefill": None if pre is None else pre["line"],
+            "mixed": None if mx is None else mx["line"],
             "copy_blocks": None if cb is None else cb["line"]}
     print(json.dumps(line), flush=True)
 

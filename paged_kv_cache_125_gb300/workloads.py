@@ -280,6 +280,64 @@ def decode_workload(name: str, context_lens: list[int], num_heads: int, num_kv_h
                     history_k=hk, history_v=hv, description=description)
 
 
+def mixed_workload(name: str, chunks: list[tuple[int, int]], decode_context_lens: list[int],
+                   num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                   num_blocks: int, device="cpu", description: str = "") -> Workload:
+    """One engine step that mixes chunked prefill and decode in a single varlen
+    paged attention call.  ``chunks`` are (length after this step, tokens
+    already in the cache) per prefilling sequence: the step queries the chunk
+    cached .. length-1 (the boundary may fall inside a block).  Every decode
+    sequence of context L queries its last token (q_len 1, L-1 cached).  All
+    earlier tokens are history rows already in the pool; the step stores the
+    new rows of every sequence, then attends.  Block tables are consecutive
+    slices of one seeded permutation of the pool."""
+    seqs = [(L, c) for L, c in chunks] + [(L, L - 1) for L in decode_context_lens]
+    for L, c in seqs:
+        if not 0 <= c < L:
+            raise ValueError("every sequence needs at least one new token")
+    perm = torch.randperm(num_blocks, generator=generator(SEED_BLOCKS)).tolist()
+    tables = _assign_blocks(perm, [num_blocks_for(L, block_size) for L, _ in seqs])
+    hist, new_slots, positions = [], [], []
+    cu_q, cu_k = [0], [0]
+    for (L, c), bt in zip(seqs, tables):
+        hist.extend(slots_of_positions(bt, range(c), block_size))
+        new_slots.extend(slots_of_positions(bt, range(c, L), block_size))
+        positions.extend(range(c, L))
+        cu_q.append(cu_q[-1] + L - c)
+        cu_k.append(cu_k[-1] + L)
+    meta = PrefillMeta(torch.tensor(cu_q, dtype=torch.int32), torch.tensor(cu_k, dtype=torch.int32),
+                       max(L - c for L, c in seqs), max(L for L, _ in seqs),
+                       torch.tensor(positions, dtype=torch.int64),
+                       torch.tensor(new_slots, dtype=torch.int32), prepare_block_tables(tables))
+    gv = generator(SEED_VALUES, device)
+    t = len(hist)
+    hk = randn_bf16((t, num_kv_heads, head_dim), gv, device)
+    hv = randn_bf16((t, num_kv_heads, head_dim), gv, device)
+    tq = cu_q[-1]
+    q = randn_bf16((tq, num_heads, head_dim), gv, device)
+    k = randn_bf16((tq, num_kv_heads, head_dim), gv, device)
+    v = randn_bf16((tq, num_kv_heads, head_dim), gv, device)
+    step = Step(StoreCall(k, v, meta.slot_mapping), PrefillCall(q, k, v, meta))
+    return Workload(name, num_heads, num_kv_heads, head_dim, block_size, num_blocks, [step],
+                    history_slots=torch.tensor(hist, dtype=torch.int64), history_k=hk, history_v=hv,
+                    description=description)
+
+
+def mixed_step_workload(device="cpu") -> Workload:
+    """Mixed step on the Qwen3-8B attention shape (32/8/128, bs 256): four
+    prompts in 1024-token chunks (first chunk of a 1024-token prompt; chunks
+    1024..2047 and 2048..3071 of longer prompts; a 700-token tail after 1300
+    cached, boundary inside a block) plus 128 decode rows with contexts
+    ~ U[512, 4096]."""
+    g = generator(SEED_LENGTHS)
+    dec = torch.randint(512, 4097, (128,), generator=g).tolist()
+    chunks = [(1024, 0), (2048, 1024), (3072, 2048), (2000, 1300)]
+    need = sum(num_blocks_for(L, 256) for L, _ in chunks) + sum(num_blocks_for(L, 256) for L in dec)
+    return mixed_workload("mixed_chunks_decode", chunks, dec, 32, 8, 128, 256, need + 64, device,
+                          description="mixed: 4 prefill chunks (3772 tokens) + 128 decode rows "
+                                      "ctx U[512,4096], 32/8/128 bs256, one varlen paged launch")
+
+
 # ---------------------------------------------------------------------------
 # The five configurations of the hot path (attention shapes of Qwen3-0.6B:
 # 16 query / 8 kv heads, and Qwen3-8B: 32 / 8 heads, head_dim 128).
