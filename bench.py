@@ -495,6 +495,50 @@ def measure_mixed(args, kvp, W, dev, stream, world, peaks):
                                    "hbm": {"achieved_gbs": round(gbs_call, 1), "algorithmic_bytes": nbytes}})}}
 
 
+def measure_bucketed(args, kvp, W, dev, stream, world, peaks):
+    """The engine's graph-replayed decode with batch-size buckets: a step of
+    50 sequences (16/8/128, bs 256, ctx U[512, 4096], 2048-block pool) copies
+    its inputs into the fixed buffers and replays the bucket-64 graph (14
+    padding rows: slot -1, context 0).  Value = algorithmic bytes of the 50
+    real sequences / step time."""
+    import torch
+    from paged_kv_cache_125_gb300.graphs import DecodeGraphs
+    g = torch.Generator().manual_seed(W.SEED_LENGTHS)
+    ctx = torch.randint(512, 4097, (50,), generator=g).tolist()
+    w = W.decode_workload("decode_b50_bucketed", ctx, 16, 8, 128, 256, 2048)
+    kc, vc = w.new_cache(dev, poison=True)
+    w.place_history(kc, vc)
+    graphs = DecodeGraphs(kc, vc, 16, 16, max_bs=64, stream=stream)
+    st, a = w.steps[0].store, w.steps[0].attn
+    ins = [a.q.to(dev), st.k.to(dev), st.v.to(dev), st.slot_mapping.to(dev),
+           a.meta.block_tables.to(dev), a.meta.context_lens.to(dev)]
+    store_b, dec_b = decode_bytes(w)
+    steps = max(100, min(2000, args.steps // 5))
+    for _ in range(max(3, args.warmup)):
+        graphs.run(*ins)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    t0.record()
+    for _ in range(steps):
+        graphs.run(*ins)
+    t1.record()
+    torch.cuda.synchronize()
+    w1 = time.perf_counter()
+    barrier(world)
+    assert kvp.device_status() == 0, "device status after the bucketed loop"
+    ms = t0.elapsed_time(t1) / steps
+    bps, ms = aggregate(store_b + dec_b, ms, world)
+    del graphs, kc, vc
+    return {"window": (w0, w1), "steps": steps,
+            "line": {"workload": "decode B50 padded to the bucket-64 graph, 16/8/128 bs256 NB2048 "
+                                 "ctx U[512,4096]", "value": round(bps / 1e9, 2), "unit": "GB/s",
+                     "ms_per_step": round(ms, 4), "steps": steps,
+                     "step": "input copies into the graph buffers + replay (kv_store + attn_decode_paged)",
+                     "frac_of_hbm": round(bps / 1e9 / peaks["hbm_gbs"], 4)}}
+
+
 def measure_copy_blocks(args, kvp, dev, stream, world, peaks):
     """Copy-on-write block copies (page 3, "场景优化1：Parallel Memory Shared"):
     one call copies 64 (src, dst) block pairs in all 56 planes of a 28-layer
@@ -568,6 +612,10 @@ def run_ours(args, rank, world, local):
     if args.only is None and not args.no_prefill:
         mx = measure_mixed(args, kvp, W, dev, stream, world, peaks)
         windows.append(mx["window"])
+    bk = None
+    if args.only is None:
+        bk = measure_bucketed(args, kvp, W, dev, stream, world, peaks)
+        windows.append(bk["window"])
     cb = None
     if args.only is None and not args.no_copy_blocks:
         cb = measure_copy_blocks(args, kvp, dev, stream, world, peaks)
@@ -598,7 +646,8 @@ def run_ours(args, rank, world, local):
             "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
             "gpu_launches": 3 * args.steps + (0 if pre is None else 2 * pre["line"]["steps"])
                             + (0 if cb is None else cb["line"]["steps"])
-                            + (0 if mx is None else 2 * mx["steps"]),
+                            + (0 if mx is None else 2 * mx["steps"])
+                            + (0 if bk is None else 3 * bk["steps"]),
             "gpu_launches_by_region": {"decode": {"kv_store": args.steps, "decode_split": args.steps,
                                                   "decode_merge": args.steps},
                                        "prefill": None if pre is None else
@@ -607,10 +656,14 @@ def run_ours(args, rank, world, local):
                                        "copy_blocks": None if cb is None else
                                        {"kv_copy_blocks": cb["line"]["steps"]},
                                        "mixed": None if mx is None else
-                                       {"kv_store": mx["steps"], "prefill": mx["steps"]}},
+                                       {"kv_store": mx["steps"], "prefill": mx["steps"]},
+                                       "decode_bucketed": None if bk is None else
+                                       {"kv_store": bk["steps"], "decode_split": bk["steps"],
+                                        "decode_merge": bk["steps"]}},
             "clocks": clocks,
             "prefill": None if pre is None else pre["line"],
             "mixed": None if mx is None else mx["line"],
+            "decode_bucketed": None if bk is None else bk["line"],
             "copy_blocks": None if cb is None else cb["line"]}
     print(json.dumps(line), flush=True)
 

@@ -1,0 +1,114 @@
+"""CUDA-graph decode with batch-size buckets, the way the pages' engine runs
+decode steps ("nano-vLLM-1", ModelRunner: graphs captured for batch sizes
+1, 2, 4, 8, 16, 32, ... up to max_num_seqs; a step of b sequences replays the
+graph of the smallest bucket >= b after copying its inputs into the graph's
+fixed buffers; the unused rows are padding: slot_mapping -1, context_lens 0).
+
+Every launch in a captured graph is a library call (``kv_store`` then
+``attn_decode_paged``); the launch configuration depends only on the bucket
+and the fixed capacities, never on the step's data, so one capture serves
+every step.  Padding rows write nothing (slot -1) and read nothing (context
+0), and their output rows are zero.
+"""
+from __future__ import annotations
+
+from . import attn_decode_paged, attn_decode_workspace_size, kv_store
+
+
+def default_buckets(max_bs: int) -> list[int]:
+    """1, 2, 4, 8, then multiples of 16 up to max_bs (the pages' list)."""
+    b = [x for x in (1, 2, 4, 8) if x <= max_bs]
+    b += list(range(16, max_bs + 1, 16))
+    if not b or b[-1] != max_bs:
+        b.append(max_bs)
+    return b
+
+
+def bucket_for(buckets: list[int], b: int) -> int:
+    """Smallest bucket >= b."""
+    for x in buckets:
+        if x >= b:
+            return x
+    raise ValueError(f"batch of {b} exceeds the largest bucket {buckets[-1]}")
+
+
+class DecodeGraphs:
+    """Captured store + decode graphs for one layer's cache.
+
+    ``k_cache`` / ``v_cache``: [num_blocks, block_size, num_kv_heads, head_dim]
+    bf16.  ``max_blocks_per_seq`` fixes the block-table width and the context
+    capacity (max_blocks_per_seq * block_size) the graphs are planned for."""
+
+    def __init__(self, k_cache, v_cache, num_heads: int, max_blocks_per_seq: int,
+                 max_bs: int = 512, buckets: list[int] | None = None,
+                 softmax_scale: float | None = None, stream=None):
+        import torch
+        self.k_cache, self.v_cache = k_cache, v_cache
+        nb, bs, hkv, d = k_cache.shape
+        dev = k_cache.device
+        self.num_heads, self.num_kv_heads, self.head_dim, self.block_size = num_heads, hkv, d, bs
+        self.max_bs = max_bs
+        self.buckets = buckets or default_buckets(max_bs)
+        if self.buckets[-1] > max_bs:
+            raise ValueError("a bucket exceeds max_bs")
+        self.capacity = max_blocks_per_seq * bs
+        self.scale = softmax_scale if softmax_scale is not None else d ** -0.5
+        bf16, i32 = torch.bfloat16, torch.int32
+        self.q = torch.zeros((max_bs, num_heads, d), dtype=bf16, device=dev)
+        self.k = torch.zeros((max_bs, hkv, d), dtype=bf16, device=dev)
+        self.v = torch.zeros((max_bs, hkv, d), dtype=bf16, device=dev)
+        self.slots = torch.full((max_bs,), -1, dtype=i32, device=dev)
+        self.block_tables = torch.zeros((max_bs, max_blocks_per_seq), dtype=i32, device=dev)
+        self.context_lens = torch.zeros((max_bs,), dtype=i32, device=dev)
+        self.out = torch.zeros((max_bs, num_heads, d), dtype=bf16, device=dev)
+        ws_bytes = attn_decode_workspace_size(max_bs, num_heads, d, self.capacity, bs)
+        self.workspace = torch.empty((max(ws_bytes, 1),), dtype=torch.uint8, device=dev)
+        self.stream = stream or torch.cuda.Stream(dev)
+        self.graphs = {}
+        for b in self.buckets:
+            self.graphs[b] = self._capture(b)
+
+    def _step(self, b: int) -> None:
+        kv_store(self.k[:b], self.v[:b], self.slots[:b], self.k_cache, self.v_cache)
+        attn_decode_paged(self.q[:b], self.k_cache, self.v_cache, self.block_tables[:b],
+                          self.context_lens[:b], self.capacity, softmax_scale=self.scale,
+                          workspace=self.workspace, out=self.out[:b])
+
+    def _capture(self, b: int):
+        import torch
+        cur = torch.cuda.current_stream()
+        self.stream.wait_stream(cur)
+        with torch.cuda.stream(self.stream):
+            self._step(b)  # warm-up outside the capture (library load, tensor maps)
+        torch.cuda.current_stream().wait_stream(self.stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            self._step(b)
+        return g
+
+    def bucket(self, b: int) -> int:
+        return bucket_for(self.buckets, b)
+
+    def run(self, q, k, v, slot_mapping, block_tables, context_lens):
+        """One decode step of b = q.shape[0] sequences: store their new K/V rows
+        at slot_mapping, attend over context_lens through block_tables.
+        Returns a view of the first b output rows (valid until the next run)."""
+        b = q.shape[0]
+        pb = self.bucket(b)
+        w = block_tables.shape[1]
+        if w > self.block_tables.shape[1]:
+            raise ValueError("block table wider than max_blocks_per_seq")
+        # No host read of context_lens (that would synchronise every step): a
+        # context above the capacity is caught by the kernel, which skips the
+        # row and sets KVP_ERR_DEVICE_DATA in the device status.
+        self.q[:b].copy_(q)
+        self.k[:b].copy_(k)
+        self.v[:b].copy_(v)
+        self.slots[:b].copy_(slot_mapping)
+        self.block_tables[:b, :w].copy_(block_tables)
+        self.context_lens[:b].copy_(context_lens)
+        if pb > b:  # padding rows: write nothing, read nothing
+            self.slots[b:pb].fill_(-1)
+            self.context_lens[b:pb].fill_(0)
+        self.graphs[pb].replay()
+        return self.out[:b]
