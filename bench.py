@@ -539,6 +539,54 @@ def measure_bucketed(args, kvp, W, dev, stream, world, peaks):
                      "frac_of_hbm": round(bps / 1e9 / peaks["hbm_gbs"], 4)}}
 
 
+def measure_scheduler():
+    """Host step loop of the engine-trace configuration (256 requests, 768
+    blocks of 256 tokens, max 512 seqs / 16384 tokens per step, 1371 steps):
+    schedule + metadata + postprocess per step, native C++ scheduler (through
+    its C ABI) against the Python replica of the same policy."""
+    from paged_kv_cache_125_gb300 import engine_trace as E
+    from paged_kv_cache_125_gb300 import workloads as W
+    from paged_kv_cache_125_gb300.scheduler import NativeScheduler
+    reqs = E.make_requests(256, (100, 1024), (100, 1024))
+
+    def py_loop():
+        sch = E.Scheduler(512, 16384, 768, 256)
+        for i, (t, o) in enumerate(reqs):
+            sch.add(E.Sequence(i, t, o, 256))
+        n = 0
+        while not sch.is_finished():
+            seqs, pre = sch.schedule()
+            lens, tabs = [len(x) for x in seqs], [list(x.block_table) for x in seqs]
+            if pre:
+                W.prefill_metadata(lens, [x.num_cached_tokens for x in seqs], tabs, 256)
+            else:
+                W.decode_metadata(lens, tabs, 256)
+            sch.postprocess(seqs, [E.synthetic_token(x.seq_id, len(x)) for x in seqs])
+            n += 1
+        return n
+
+    def native_loop():
+        sch = NativeScheduler(768, 256, 512, 16384)
+        for i, (t, o) in enumerate(reqs):
+            sch.add(i, t, o)
+        n = 0
+        while not sch.is_finished():
+            ids, _, _ = sch.step()
+            sch.postprocess([(7 * i + n) % 151936 for i in ids])
+            n += 1
+        return n
+
+    out = {}
+    for name, f in (("native", native_loop), ("python_replica", py_loop)):
+        t0 = time.perf_counter()
+        n = f()
+        out[name] = round((time.perf_counter() - t0) / n * 1e6, 1)
+        out["steps"] = n
+    return {"workload": "engine trace: 256 requests, 768 blocks x 256 tokens, 512 seqs / 16384 tokens per step",
+            "unit": "us/step (host: schedule + metadata + postprocess)",
+            "native": out["native"], "python_replica": out["python_replica"], "steps": out["steps"]}
+
+
 def measure_copy_blocks(args, kvp, dev, stream, world, peaks):
     """Copy-on-write block copies (page 3, "场景优化1：Parallel Memory Shared"):
     one call copies 64 (src, dst) block pairs in all 56 planes of a 28-layer
@@ -663,6 +711,7 @@ def run_ours(args, rank, world, local):
             "clocks": clocks,
             "prefill": None if pre is None else pre["line"],
             "mixed": None if mx is None else mx["line"],
+            "scheduler": measure_scheduler() if args.only is None else None,
             "decode_bucketed": None if bk is None else bk["line"],
             "copy_blocks": None if cb is None else cb["line"]}
     print(json.dumps(line), flush=True)

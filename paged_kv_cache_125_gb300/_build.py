@@ -1,6 +1,6 @@
 """Builds libkvpaged.so in-tree with nvcc for sm_103a (no cmake, no torch extension).
 
-Each .cu file is compiled in parallel to an object, then linked into
+Each .cu (and host-only .cpp) file is compiled in parallel to an object, then linked into
 paged_kv_cache_125_gb300/_build/libkvpaged.so.  A rebuild happens only when a
 source or header is newer than the library.
 """
@@ -29,7 +29,7 @@ def nvcc() -> str:
 
 
 def sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _stale() -> bool:
@@ -50,7 +50,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(OUT, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(OUT, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc(), "-c", src, "-o", obj] + flags
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
