@@ -66,6 +66,8 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-copy-blocks", action="store_true")
+    p.add_argument("--no-large", action="store_true", help="skip the 150 GB decode B512 line")
+    p.add_argument("--no-trace", action="store_true", help="skip the engine-trace replay line")
     p.add_argument("--only", choices=["decode", "prefill"], default=None,
                    help="run one half only (profiling); the JSON line then carries that half")
     p.add_argument("--sets", type=int, default=N_SETS, help="input sets in rotation")
@@ -539,6 +541,124 @@ def measure_bucketed(args, kvp, W, dev, stream, world, peaks):
                      "frac_of_hbm": round(bps / 1e9 / peaks["hbm_gbs"], 4)}}
 
 
+def measure_decode_large(args, kvp, W, dev, stream, world, peaks):
+    """The bandwidth sweep configuration: 512 sequences, Qwen3-8B heads
+    (32/8/128), bs 256, contexts 50% U[128, 1024] + 50% U[4096, 8192], over a
+    143,051-block pool (150 GB of K+V, unreferenced blocks NaN).  One input set
+    (the step reads ~7 GB, 55x the L2); store + decode graphs as in the main
+    line."""
+    import torch
+    torch.cuda.empty_cache()
+    free, _ = torch.cuda.mem_get_info(dev)
+    if free < 165e9:
+        return {"window": None, "steps": 0,
+                "line": {"skipped": f"needs ~160 GB free device memory, {free / 1e9:.0f} GB free"}}
+    w = W.config4_decode(device=dev)
+    store_b, dec_b = decode_bytes(w)
+    ds = DeviceSet(w, dev)
+    m = w.steps[0].attn.meta
+    ws = torch.empty(kvp.attn_decode_workspace_size(512, 32, 128, m.max_context_len, 256),
+                     dtype=torch.uint8, device=dev)
+    sg = capture(lambda s_: store_call(kvp, s_), [ds], stream)
+    dg = capture(lambda s_: decode_call(kvp, s_, w, ws), [ds], stream)
+    steps = max(10, min(100, args.steps // 100))
+    ms_step, ms_dec, win = timed_loop(sg, dg, steps, max(3, args.warmup // 4), world)
+    assert kvp.device_status() == 0, "device status after the large decode loop"
+    bps, ms_step = aggregate(store_b + dec_b, ms_step, world)
+    achieved = dec_b / (ms_dec * 1e-3) / 1e9
+    del sg, dg, ds, ws
+    torch.cuda.empty_cache()
+    return {"window": win, "steps": steps,
+            "line": {"workload": w.description, "value": round(bps / 1e9, 2), "unit": "GB/s",
+                     "ms_per_step": round(ms_step, 4), "steps": steps,
+                     "step": "kv_store (512 new rows) + attn_decode_paged",
+                     "roofline": {"kernel": "attn_decode_paged (split + merge)", "bound": "hbm",
+                                  "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                                  "algorithmic_bytes": dec_b, "peak_source": peaks["source"],
+                                  "ms_per_launch": round(ms_dec, 5)}}}
+
+
+def measure_trace(args, kvp, dev, stream, world, peaks):
+    """Engine-trace replay: 256 requests (prompts and outputs U[100, 1024]),
+    scheduled by the native scheduler (prefill first, max 512 seqs / 16384
+    tokens per step, 768 blocks of 256 tokens), every step running kv_store +
+    prefill or decode attention on all 28 layers of a Qwen3-0.6B attention
+    shape (16/8/128).  Aggregate GB/s over the decode steps (algorithmic
+    bytes) and TFLOP/s over the prefill steps (causal FLOPs), each timed by an
+    event pair around the step's 28 layers."""
+    import torch
+    from paged_kv_cache_125_gb300 import engine_trace as E
+    from paged_kv_cache_125_gb300.scheduler import NativeScheduler
+    layers, hq, hkv, d, bs, nb = 28, 16, 8, 128, 256, 768
+    scale = d ** -0.5
+    torch.cuda.empty_cache()
+    kv = torch.full((2, layers, nb, bs, hkv, d), float("nan"), dtype=torch.bfloat16, device=dev)
+    sch = NativeScheduler(nb, bs, 512, 16384)
+    for i, (t, o) in enumerate(E.make_requests(256, (100, 1024), (100, 1024))):
+        sch.add(i, t, o)
+    gq = torch.Generator(device=dev).manual_seed(5)
+    row = hkv * d * 2
+    ws = torch.empty(kvp.attn_decode_workspace_size(512, hq, d, 4096, bs), dtype=torch.uint8, device=dev)
+    recs = []
+    w0 = time.perf_counter()
+    while not sch.is_finished():
+        ids, pre, m = sch.step()
+        n = int(m.cu_seqlens_q[-1]) if pre else len(ids)
+        q = torch.randn((n, hq, d), generator=gq, device=dev).to(torch.bfloat16)
+        k = torch.randn((n, hkv, d), generator=gq, device=dev).to(torch.bfloat16)
+        v = torch.randn((n, hkv, d), generator=gq, device=dev).to(torch.bfloat16)
+        slots = m.slot_mapping.to(dev, non_blocking=True)
+        if pre:
+            cq, ck = m.cu_seqlens_q.to(dev, non_blocking=True), m.cu_seqlens_k.to(dev, non_blocking=True)
+            bt = None if m.block_tables is None else m.block_tables.to(dev, non_blocking=True)
+            ql = (m.cu_seqlens_q[1:] - m.cu_seqlens_q[:-1]).long()
+            kl = (m.cu_seqlens_k[1:] - m.cu_seqlens_k[:-1]).long()
+            work = 4 * d * hq * int((ql * (kl - ql) + ql * (ql + 1) // 2).sum())
+        else:
+            bt, ctx = m.block_tables.to(dev, non_blocking=True), m.context_lens.to(dev, non_blocking=True)
+            c = m.context_lens.long()
+            work = 4 * n * row + int(c.sum()) * row * 2 + 2 * n * hq * d * 2 + \
+                int(((c + bs - 1) // bs).sum()) * 4 + n * 4
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for layer in range(layers):
+            kc, vc = kv[0, layer], kv[1, layer]
+            kvp.kv_store(k, v, slots, kc, vc)
+            if pre:
+                kvp.attn_prefill_varlen(q, cq, ck, m.max_seqlen_q, m.max_seqlen_k, k=k, v=v, k_cache=kc,
+                                        v_cache=vc, block_tables=bt, num_kv_heads=hkv, softmax_scale=scale)
+            else:
+                kvp.attn_decode_paged(q, kc, vc, bt, ctx, m.max_context_len, softmax_scale=scale,
+                                      workspace=ws)
+        b.record()
+        recs.append((pre, work * layers, a, b))
+        sch.postprocess([(7 * i + n) % 151936 for i in ids])
+    torch.cuda.synchronize()
+    w1 = time.perf_counter()
+    assert kvp.device_status() == 0, "device status after the trace replay"
+    dec_ms = sum(a.elapsed_time(b) for p_, _, a, b in recs if not p_)
+    pre_ms = sum(a.elapsed_time(b) for p_, _, a, b in recs if p_)
+    dec_work = sum(w_ for p_, w_, _, _ in recs if not p_)
+    pre_work = sum(w_ for p_, w_, _, _ in recs if p_)
+    n_dec = sum(1 for r in recs if not r[0])
+    del kv, ws
+    torch.cuda.empty_cache()
+    dec_gbs = dec_work / (dec_ms * 1e-3) / 1e9
+    pre_tf = pre_work / (pre_ms * 1e-3) / 1e12
+    return {"window": (w0, w1), "launches": 2 * layers * len(recs) + layers * n_dec,
+            "line": {"workload": "engine trace: 256 requests, prompts/outputs U[100,1024], 28 layers "
+                                 "16/8/128, bs 256, 768 blocks, native scheduler",
+                     "steps": len(recs), "decode_steps": n_dec, "prefill_steps": len(recs) - n_dec,
+                     "preemptions": sch.num_preemptions,
+                     "decode": {"value": round(dec_gbs, 2), "unit": "GB/s", "ms": round(dec_ms, 2),
+                                "frac_of_hbm": round(dec_gbs / peaks["hbm_gbs"], 4)},
+                     "prefill": {"value": round(pre_tf, 2), "unit": "TFLOP/s", "ms": round(pre_ms, 2),
+                                 "frac_of_bf16_burst": round(pre_tf / peaks["bf16_tflops"], 4)},
+                     "how": "event pair around each step's 28 layers (store + attention); "
+                            "inputs generated on the device before each step"}}
+
+
 def measure_scheduler():
     """Host step loop of the engine-trace configuration (256 requests, 768
     blocks of 256 tokens, max 512 seqs / 16384 tokens per step, 1371 steps):
@@ -668,6 +788,15 @@ def run_ours(args, rank, world, local):
     if args.only is None and not args.no_copy_blocks:
         cb = measure_copy_blocks(args, kvp, dev, stream, world, peaks)
         windows.append(cb["window"])
+    tr = None
+    if args.only is None and not args.no_trace:
+        tr = measure_trace(args, kvp, dev, stream, world, peaks)
+        windows.append(tr["window"])
+    dl = None
+    if args.only is None and not args.no_large:
+        dl = measure_decode_large(args, kvp, W, dev, stream, world, peaks)
+        if dl["window"] is not None:
+            windows.append(dl["window"])
     time.sleep(0.1)
     clocks = sampler.stop(windows)
 
@@ -695,7 +824,9 @@ def run_ours(args, rank, world, local):
             "gpu_launches": 3 * args.steps + (0 if pre is None else 2 * pre["line"]["steps"])
                             + (0 if cb is None else cb["line"]["steps"])
                             + (0 if mx is None else 2 * mx["steps"])
-                            + (0 if bk is None else 3 * bk["steps"]),
+                            + (0 if bk is None else 3 * bk["steps"])
+                            + (0 if dl is None else 3 * dl["steps"])
+                            + (0 if tr is None else tr["launches"]),
             "gpu_launches_by_region": {"decode": {"kv_store": args.steps, "decode_split": args.steps,
                                                   "decode_merge": args.steps},
                                        "prefill": None if pre is None else
@@ -705,6 +836,10 @@ def run_ours(args, rank, world, local):
                                        {"kv_copy_blocks": cb["line"]["steps"]},
                                        "mixed": None if mx is None else
                                        {"kv_store": mx["steps"], "prefill": mx["steps"]},
+                                       "engine_trace": None if tr is None else {"all": tr["launches"]},
+                                       "decode_b512": None if dl is None or not dl["steps"] else
+                                       {"kv_store": dl["steps"], "decode_split": dl["steps"],
+                                        "decode_merge": dl["steps"]},
                                        "decode_bucketed": None if bk is None else
                                        {"kv_store": bk["steps"], "decode_split": bk["steps"],
                                         "decode_merge": bk["steps"]}},
@@ -713,6 +848,8 @@ def run_ours(args, rank, world, local):
             "mixed": None if mx is None else mx["line"],
             "scheduler": measure_scheduler() if args.only is None else None,
             "decode_bucketed": None if bk is None else bk["line"],
+            "decode_b512": None if dl is None else dl["line"],
+            "engine_trace": None if tr is None else tr["line"],
             "copy_blocks": None if cb is None else cb["line"]}
     print(json.dumps(line), flush=True)
 

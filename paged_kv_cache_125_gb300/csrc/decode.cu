@@ -34,9 +34,23 @@
 namespace kvp {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kBaseWarps = 8;  // consumer warps before the head split
 constexpr int kStages = 6;
+
+// Query heads of a kv head are split over HS warps when a warp holding all
+// G of them would need G * D / 8 query floats plus as many accumulators per
+// lane (G * D >= 512): each warp then owns G / HS heads, so its query and
+// accumulators stay in registers and twice as many warps hide the latency of
+// the dot products.  HS = 2 gives 16 consumer warps + the producer: 17 warps,
+// 5 on one SM sub-partition, so at most 16384 / (5 * 32) = 102 registers.
+template <int D, int G>
+__host__ __device__ constexpr int head_split() {
+  return G * D >= 512 ? 2 : 1;
+}
+template <int HS>
+__host__ __device__ constexpr int consumer_warps() {
+  return kBaseWarps * HS;
+}
 constexpr int kTokensAllHeads = 64;  // tokens * kv heads per stage
 
 // Row of one split partial in the workspace: accumulator[D], m, l, and two pad
@@ -100,10 +114,10 @@ __host__ __device__ constexpr bool q_in_smem() {
 
 template <int D, int G>
 __host__ __device__ constexpr size_t decode_smem_bytes() {
+  constexpr int HS = head_split<D, G>(), CW = consumer_warps<HS>(), GE = G / HS;
   return 2 * kStages * stage_half_bytes<D>() + kStages * sizeof(StageMeta) +
-         (2 * kStages + 2 * kConsumerWarps) * sizeof(uint64_t) +
-         (size_t)kConsumerWarps * G * (D + 2) * sizeof(float) +
-         (q_in_smem<D, G>() ? (size_t)kConsumerWarps * G * D * sizeof(float) : 0);
+         (2 * kStages + 2 * CW) * sizeof(uint64_t) + (size_t)CW * GE * (D + 2) * sizeof(float) +
+         (q_in_smem<D, GE>() ? (size_t)CW * GE * D * sizeof(float) : 0);
 }
 
 // ---------------------------------------------------------------- producer
@@ -236,7 +250,9 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* ringK, uint8_t* ri
 
 // ---------------------------------------------------------------- consumers
 
-template <int D, int G>
+// Template G here is the number of query heads this warp owns (the group
+// size divided by the head split HS); hs selects which part of the group.
+template <int D, int G, int HS>
 __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const uint8_t* ringV,
                                 const StageMeta* meta, uint64_t* full, uint64_t* empty,
                                 uint64_t* xfull, uint64_t* xfree, float* xw, float* qs_all) {
@@ -244,8 +260,11 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
   constexpr bool kQS = q_in_smem<D, G>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = a.num_kv_heads;
-  const int NS = kConsumerWarps / Hkv;
-  const int g = warp % Hkv, sub = warp / Hkv;
+  const int NS = kBaseWarps / Hkv;
+  const int hs = warp % HS, wb = warp / HS;
+  const int g = wb % Hkv, sub = wb / Hkv;
+  const int head0 = (g * HS + hs) * G;  // first query head of this warp
+  const int xi = g * HS + hs;           // hand-off barriers of (kv head, head part)
   const int li = lane & 7, tg = lane >> 3;
   const int row_elems = Hkv * D;
 
@@ -266,7 +285,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
 
     if (md.flags & F_NEW) {
       b = md.b;
-      const uint16_t* qrow = a.q + (int64_t)b * a.q_stride + (int64_t)g * G * D;
+      const uint16_t* qrow = a.q + (int64_t)b * a.q_stride + (int64_t)head0 * D;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
 #pragma unroll
@@ -328,9 +347,12 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
             for (int e = 0; e < 8; ++e) qv[e] = qf[kQS ? 0 : h][c][e];
           }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            acc0 = fmaf(qv[2 * e], bf16lo(w[e]), acc0);
-            acc1 = fmaf(qv[2 * e + 1], bf16hi(w[e]), acc1);
+          for (int e = 0; e < 4; ++e) {  // packed fp32x2 FMA: elements 2e, 2e+1
+            const float2 r = __ffma2_rn(make_float2(qv[2 * e], qv[2 * e + 1]),
+                                        make_float2(bf16lo(w[e]), bf16hi(w[e])),
+                                        make_float2(acc0, acc1));
+            acc0 = r.x;
+            acc1 = r.y;
           }
         }
         float x = acc0 + acc1;
@@ -377,8 +399,11 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
         for (int h = 0; h < G; ++h)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            acc[h][c][2 * e] = fmaf(pr[p][h], bf16lo(w[e]), acc[h][c][2 * e]);
-            acc[h][c][2 * e + 1] = fmaf(pr[p][h], bf16hi(w[e]), acc[h][c][2 * e + 1]);
+            const float2 r = __ffma2_rn(make_float2(pr[p][h], pr[p][h]),
+                                        make_float2(bf16lo(w[e]), bf16hi(w[e])),
+                                        make_float2(acc[h][c][2 * e], acc[h][c][2 * e + 1]));
+            acc[h][c][2 * e] = r.x;
+            acc[h][c][2 * e + 1] = r.y;
           }
       }
     }
@@ -413,7 +438,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
       // the buffer through xfree[g] before the next segment's hand-off.
       writer = sub == 0;
       if (!writer) {
-        if (seg > 0 && !mbar_wait(&xfree[g], (uint32_t)((seg - 1) & 1), a.status)) return;
+        if (seg > 0 && !mbar_wait(&xfree[xi], (uint32_t)((seg - 1) & 1), a.status)) return;
         float* mine = xw + (size_t)warp * G * (D + 2);
         if (tg == 0) {
 #pragma unroll
@@ -429,14 +454,14 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&xfull[g]);
+        if (lane == 0) mbar_arrive(&xfull[xi]);
       } else {
-        if (!mbar_wait(&xfull[g], (uint32_t)(seg & 1), a.status)) return;
+        if (!mbar_wait(&xfull[xi], (uint32_t)(seg & 1), a.status)) return;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           float M = m[h];
           for (int k = 1; k < NS; ++k)
-            M = fmaxf(M, xw[(size_t)(g + k * Hkv) * G * (D + 2) + h * (D + 2) + D]);
+            M = fmaxf(M, xw[(size_t)((g + k * Hkv) * HS + hs) * G * (D + 2) + h * (D + 2) + D]);
           const float Mu = M == -INFINITY ? 0.f : M;
           const float w0 = fast_exp2(m[h] - Mu);
           float ls = w0 * l[h];
@@ -445,7 +470,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[h][c][e] *= w0;
           for (int k = 1; k < NS; ++k) {
-            const float* o = xw + (size_t)(g + k * Hkv) * G * (D + 2) + h * (D + 2);
+            const float* o = xw + (size_t)((g + k * Hkv) * HS + hs) * G * (D + 2) + h * (D + 2);
             const float w = fast_exp2(o[D] - Mu);
             ls += w * o[D + 1];
 #pragma unroll
@@ -457,7 +482,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
           l[h] = ls;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&xfree[g]);
+        if (lane == 0) mbar_arrive(&xfree[xi]);
       }
     }
     ++seg;
@@ -467,7 +492,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float inv = 1.f / l[h];
-        uint16_t* orow = a.out + (int64_t)b * a.out_stride + (int64_t)(g * G + h) * D;
+        uint16_t* orow = a.out + (int64_t)b * a.out_stride + (int64_t)(head0 + h) * D;
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
           uint4 u;
@@ -483,7 +508,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float* dst =
-            a.part + (((size_t)blockIdx.x * 2 + slot) * a.num_heads + g * G + h) * part_stride<D>();
+            a.part + (((size_t)blockIdx.x * 2 + slot) * a.num_heads + head0 + h) * part_stride<D>();
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
           float4* d4 = reinterpret_cast<float4*>(dst + (c * 8 + li) * 8);
@@ -499,8 +524,9 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
   }
 }
 
-template <int D, int G>
-__global__ void __maxnreg__(168) decode_split_kernel(const DecodeArgs a) {
+template <int D, int G, int HS>
+__global__ void __maxnreg__(HS == 1 ? 168 : 96) decode_split_kernel(const DecodeArgs a) {
+  constexpr int CW = consumer_warps<HS>(), GE = G / HS;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ringK = smem;
   uint8_t* ringV = smem + kStages * stage_half_bytes<D>();
@@ -508,29 +534,29 @@ __global__ void __maxnreg__(168) decode_split_kernel(const DecodeArgs a) {
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + kStages);
   uint64_t* empty = full + kStages;
   uint64_t* xfull = empty + kStages;
-  uint64_t* xfree = xfull + kConsumerWarps;
-  float* xw = reinterpret_cast<float*>(xfree + kConsumerWarps);
-  float* qs = xw + (size_t)kConsumerWarps * G * (D + 2);
+  uint64_t* xfree = xfull + CW;
+  float* xw = reinterpret_cast<float*>(xfree + CW);
+  float* qs = xw + (size_t)CW * GE * (D + 2);
 
   if (threadIdx.x == 0) {
     // The merge kernel may be scheduled now; it waits for this grid to finish.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kConsumerWarps);
+      mbar_init(&empty[i], CW);
     }
-    const int ns = kConsumerWarps / a.num_kv_heads;
-    for (int i = 0; i < kConsumerWarps; ++i) {
+    const int ns = kBaseWarps / a.num_kv_heads;
+    for (int i = 0; i < CW; ++i) {
       mbar_init(&xfull[i], ns > 1 ? ns - 1 : 1);
       mbar_init(&xfree[i], 1);
     }
     fence_mbar_init();
   }
   __syncthreads();
-  if ((threadIdx.x >> 5) == kConsumerWarps)
+  if ((threadIdx.x >> 5) == CW)
     decode_producer<D>(a, ringK, ringV, meta, full, empty);
   else
-    decode_consumer<D, G>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
+    decode_consumer<D, GE, HS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
 }
 
 // Combines the partials of every sequence that crosses a CTA boundary.
@@ -569,11 +595,12 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const float* __restrict
 
 template <int D, int G>
 cudaError_t launch_decode_t(const DecodeArgs& a, int ctas, cudaStream_t stream) {
+  constexpr int HS = head_split<D, G>();
   const size_t smem = decode_smem_bytes<D, G>();
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, HS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_split_kernel<D, G><<<ctas, kThreads, smem, stream>>>(a);
+  decode_split_kernel<D, G, HS><<<ctas, (consumer_warps<HS>() + 1) * 32, smem, stream>>>(a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
