@@ -12,7 +12,11 @@ rotation, so no step finds its inputs in L2 (8.6 GB footprint vs 126 MB L2).
 value = algorithmic bytes of the step (K/V of every context token read once,
 q, out, new rows stored, block-table entries, context_lens) / step time, in
 GB/s.  The same line carries the prefill half of the metric (varlen prefill
-with prefix cache, 8 prompts, Qwen3-8B heads): causal FLOPs / time.
+with prefix cache, 8 prompts, Qwen3-8B heads): causal FLOPs / time, with the
+prefill steps launched eagerly (the pages' engine graph-replays decode only),
+and further lines: a mixed chunked-prefill + decode step, bucketed graph
+decode, copy-on-write block copies, the 150 GB decode B512 sweep, the
+28-layer engine-trace replay and the host scheduler step loop.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -46,12 +50,12 @@ N_SETS = 4
 TRAFFIC = {
     # decode B64 workload (one input set), one ncu --set full capture of the split kernel
     "decode": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu",
-               "sha256": "c83d43b4f15bd4c86b53010a9cb312d104ffad5357352bf404658ab3274b97a0",
-               "bytes": 569101824 + 4088064},
+               "sha256": "b88bad612cfecedb310bc514a21e8cb90a381ac7248bd2168639ae5888215b46",
+               "bytes": 569084160 + 4334848},
     # prefill workload (8 prompts, 32/8/128), one ncu --set full capture
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
-                "sha256": "12dbff6aef6fea57751e9b2472606cb49331b35736521816defd51a925b687de",
-                "bytes": 122565888 + 33760256},
+                "sha256": "e860c116ff6772463152811a00018182a6972dc0befc488142f378267eee78ad",
+                "bytes": 122845696 + 33512704},
 }
 
 
@@ -304,6 +308,36 @@ def timed_loop(store_graphs, attn_graphs, steps, warmup, world):
     return ms_step, statistics.mean(durs), (w0, w1)
 
 
+def timed_loop_eager(store_fn, attn_fn, sets, steps, warmup, world):
+    """As timed_loop, with the two calls launched directly (no graph): the
+    pages' engine runs prefill steps eagerly and graph-replays only decode."""
+    import torch
+    n = len(sets)
+    for i in range(warmup):
+        store_fn(sets[i % n])
+        attn_fn(sets[i % n])
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    start.record()
+    for i in range(steps):
+        store_fn(sets[i % n])
+        evs[i][0].record()
+        attn_fn(sets[i % n])
+        evs[i][1].record()
+    stop.record()
+    torch.cuda.synchronize()
+    w1 = time.perf_counter()
+    barrier(world)
+    ms_step = start.elapsed_time(stop) / steps
+    durs = [a.elapsed_time(b) for a, b in evs]
+    return ms_step, statistics.mean(durs), (w0, w1)
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 
 def oracle_decode_rate(w, min_seconds=8.0):
@@ -431,18 +465,19 @@ def measure_prefill(args, kvp, W, dev, stream, world, peaks):
     wp = W.config3_prefill()
     flops = prefill_flops(wp)
     psets = [DeviceSet(wp, dev) for _ in range(args.sets)]
-    pstore = capture(lambda s: store_call(kvp, s), psets, stream)
-    pattn = capture(lambda s: prefill_call(kvp, s, wp), psets, stream)
     psteps = args.prefill_steps or max(50, args.steps // 4)
-    ms_pstep, ms_prefill, pwin = timed_loop(pstore, pattn, psteps, args.warmup, world)
+    ms_pstep, ms_prefill, pwin = timed_loop_eager(lambda s_: store_call(kvp, s_),
+                                                  lambda s_: prefill_call(kvp, s_, wp), psets, psteps,
+                                                  args.warmup, world)
     assert kvp.device_status() == 0, "device status after the timed prefill loop"
     flops_per_s, ms_pstep = aggregate(flops, ms_pstep, world)
     tflops_kernel = flops / (ms_prefill * 1e-3) / 1e12
-    del pstore, pattn, psets
+    del psets
     return {"window": pwin,
             "line": {"workload": wp.description, "value": round(flops_per_s / 1e12, 2),
                      "unit": "TFLOP/s", "ms_per_step": round(ms_pstep, 4), "steps": psteps,
-                     "step": "kv_store of the uncached suffix + attn_prefill_varlen (paged, prefix cache)",
+                     "step": "kv_store of the uncached suffix + attn_prefill_varlen (paged, prefix cache), "
+                             "launched eagerly as the engine runs prefill steps",
                      "roofline": {"kernel": "attn_prefill_varlen", "bound": "tensor",
                                   "achieved": round(tflops_kernel, 1), "peak": peaks["bf16_tflops"],
                                   "unit": "TFLOP/s", "frac": round(tflops_kernel / peaks["bf16_tflops"], 4),
@@ -454,8 +489,8 @@ def measure_prefill(args, kvp, W, dev, stream, world, peaks):
 def measure_mixed(args, kvp, W, dev, stream, world, peaks):
     """One engine step mixing chunked prefill and decode in a single varlen
     paged prefill call (4 prompt chunks, 3772 tokens, + 128 decode rows,
-    32/8/128): store of the new rows + the attention call, CUDA graphs over
-    2 input sets in rotation."""
+    32/8/128): store of the new rows + the attention call, launched eagerly
+    over 2 input sets in rotation."""
     wm = W.mixed_step_workload()
     flops = prefill_flops(wm)
     m = wm.steps[0].attn.meta
@@ -464,17 +499,17 @@ def measure_mixed(args, kvp, W, dev, stream, world, peaks):
     qo_bytes = int(m.cu_seqlens_q[-1]) * wm.num_heads * wm.head_dim * 2 * 2
     nbytes = kv_bytes + qo_bytes
     msets = [DeviceSet(wm, dev) for _ in range(2)]
-    mstore = capture(lambda s: store_call(kvp, s), msets, stream)
-    mattn = capture(lambda s: prefill_call(kvp, s, wm), msets, stream)
     steps = max(50, min(400, args.steps // 10))
-    ms_step, ms_call, win = timed_loop(mstore, mattn, steps, args.warmup, world)
+    ms_step, ms_call, win = timed_loop_eager(lambda s_: store_call(kvp, s_),
+                                             lambda s_: prefill_call(kvp, s_, wm), msets, steps,
+                                             args.warmup, world)
     assert kvp.device_status() == 0, "device status after the mixed loop"
     fps, ms_step = aggregate(flops, ms_step, world)
     tf_call = flops / (ms_call * 1e-3) / 1e12
     gbs_call = nbytes / (ms_call * 1e-3) / 1e9
     # the binding roofline is the larger of the two lower bounds on the call's time
     hbm_bound = nbytes / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12)
-    del mstore, mattn, msets
+    del msets
     return {"window": win, "steps": steps,
             "line": {"workload": wm.description, "value": round(fps / 1e12, 2), "unit": "TFLOP/s",
                      "ms_per_step": round(ms_step, 4), "steps": steps,

@@ -646,7 +646,9 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
         sum2 = __fadd2_rn(sum2, p);
         pk[i] = pack_bf16x2(p.x, p.y);
       }
-      if (rescale) {  // S commit of this tile => the previous PV into O is complete
+      // tcgen05.ld/st are warp-collective (.sync.aligned): the warp takes the
+      // branch together when any of its rows rescales; the others have alpha 1.
+      if (__any_sync(0xffffffffu, rescale)) {  // S commit => previous PV into O is complete
         l *= alpha;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {

@@ -86,3 +86,28 @@ def test_prefill_out_of_range_block_is_flagged():
                             a.meta.max_seqlen_q, a.meta.max_seqlen_k, k_cache=kc, v_cache=vc,
                             block_tables=bt.cuda())
     assert kvp.device_status() == -6
+
+
+@pytest.mark.parametrize("cached_blocks,hq,hkv", [(0, 16, 8), (2, 16, 8), (2, 32, 8), (1, 8, 1)])
+def test_prefill_scores_growing_across_tiles(cached_blocks, hq, hkv):
+    """Keys whose scores rise by ~10 (log2 units) per 128-key tile: the running
+    max grows past the lazy-rescale threshold on every tile, so the O / row-sum
+    rescale path runs (warp-wide) on every tile of every row."""
+    L, d, bs = 900, 128, 128
+    nb = W.num_blocks_for(L, bs) + 3
+    w = W.prefill_workload(f"rescale_{cached_blocks}_{hq}_{hkv}", [L], [cached_blocks], hq, hkv, d,
+                           bs, nb)
+    g = torch.Generator().manual_seed(31)
+    c = cached_blocks * bs
+
+    def keys(pos):
+        p = torch.tensor(pos, dtype=torch.float32)[:, None, None]
+        return (0.02 * p * torch.ones((len(pos), hkv, d)) +
+                0.1 * torch.randn((len(pos), hkv, d), generator=g)).to(torch.bfloat16)
+
+    if c:
+        w.setup[0].k.copy_(keys(list(range(c))))
+    st, a = w.steps[0].store, w.steps[0].attn
+    st.k.copy_(keys(list(range(c, L))))
+    a.q.copy_((0.25 + 0.05 * torch.randn(a.q.shape, generator=g)).to(torch.bfloat16))
+    _check(w)
