@@ -4,10 +4,13 @@
 One step = one pass of the hot path over one batch of the decode workload
 (64 sequences, Qwen3-0.6B attention shape 16/8/128, context_lens uniform in
 [512, 4096], block_size 256, blocks shuffled over a 2048-block pool):
-kv_store of the step's 64 new K/V rows, then attn_decode_paged (split kernel +
-log-sum-exp merge).  The step is replayed from a CUDA graph (graph-safe
+kv_store of the step's 64 new K/V rows and the paged decode (split kernel +
+log-sum-exp merge), in one call (attn_decode_paged_append, the store fused
+into the decode launch).  The step is replayed from a CUDA graph (graph-safe
 decode, as the serving engine runs it) over 4 independent input sets in
 rotation, so no step finds its inputs in L2 (8.6 GB footprint vs 126 MB L2).
+The same step as two calls (kv_store, then attn_decode_paged) is reported
+beside it under "unfused".
 
 value = algorithmic bytes of the step (K/V of every context token read once,
 q, out, new rows stored, block-table entries, context_lens) / step time, in
@@ -229,6 +232,12 @@ def decode_call(kvp, s, w, ws):
                           workspace=ws, out=s.out)
 
 
+def append_call(kvp, s, w, ws):
+    """The decode step in one call: kv_store of the new rows fused into the decode."""
+    kvp.attn_decode_paged_append(s.q, s.k, s.v, s.slots, s.kc, s.vc, s.bt, s.ctx, s.max_ctx,
+                                 softmax_scale=w.scale, workspace=ws, out=s.out)
+
+
 def prefill_call(kvp, s, w):
     kvp.attn_prefill_varlen(s.q, s.cu_q, s.cu_k, s.max_q, s.max_k, k=s.k, v=s.v, k_cache=s.kc,
                             v_cache=s.vc, block_tables=s.bt, num_kv_heads=w.num_kv_heads,
@@ -298,6 +307,35 @@ def timed_loop(store_graphs, attn_graphs, steps, warmup, world):
         store_graphs[i % n].replay()
         evs[i][0].record()
         attn_graphs[i % n].replay()
+        evs[i][1].record()
+    stop.record()
+    torch.cuda.synchronize()
+    w1 = time.perf_counter()
+    barrier(world)
+    ms_step = start.elapsed_time(stop) / steps
+    durs = [a.elapsed_time(b) for a, b in evs]
+    return ms_step, statistics.mean(durs), (w0, w1)
+
+
+def timed_loop_single(graphs, steps, warmup, world):
+    """One step = one graph replay of input set i % n (the fused store +
+    decode call); an event pair around every replay gives the call's duration.
+    Returns (ms per step, mean ms of the call, wall window)."""
+    import torch
+    n = len(graphs)
+    for i in range(warmup):
+        graphs[i % n].replay()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.perf_counter()
+    start.record()
+    for i in range(steps):
+        evs[i][0].record()
+        graphs[i % n].replay()
         evs[i][1].record()
     stop.record()
     torch.cuda.synchronize()
@@ -415,19 +453,34 @@ def measure_decode(args, kvp, W, dev, stream, world, peaks):
     ws = torch.empty(kvp.attn_decode_workspace_size(64, w.num_heads, w.head_dim,
                                                     w.steps[0].attn.meta.max_context_len,
                                                     w.block_size), dtype=torch.uint8, device=dev)
-    store_graphs = capture(lambda s: store_call(kvp, s), sets, stream)
-    dec_graphs = capture(lambda s: decode_call(kvp, s, w, ws), sets, stream)
+    app_graphs = capture(lambda s: append_call(kvp, s, w, ws), sets, stream)
     assert kvp.device_status() == 0
-    ms_step, ms_decode, win = timed_loop(store_graphs, dec_graphs, args.steps, args.warmup, world)
+    ms_step, ms_call, win = timed_loop_single(app_graphs, args.steps, args.warmup, world)
     assert kvp.device_status() == 0, "device status after the timed decode loop"
     bytes_per_s, ms_step = aggregate(step_bytes, ms_step, world)
-    dec_achieved = dec_b / (ms_decode * 1e-3) / 1e9
+    achieved = step_bytes / (ms_call * 1e-3) / 1e9
     res = {"w": w, "window": win, "ms_step": ms_step, "value": bytes_per_s / 1e9,
-           "roofline": {"kernel": "attn_decode_paged (split + merge)", "bound": "hbm",
-                        "achieved": round(dec_achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                        "frac": round(dec_achieved / peaks["hbm_gbs"], 4), "traffic": traffic_for("decode"),
-                        "algorithmic_bytes": dec_b, "peak_source": peaks["source"],
-                        "ms_per_launch": round(ms_decode, 5)}}
+           "roofline": {"kernel": "attn_decode_paged_append (store + split + merge)", "bound": "hbm",
+                        "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic_for("decode"),
+                        "algorithmic_bytes": step_bytes, "peak_source": peaks["source"],
+                        "ms_per_launch": round(ms_call, 5)}}
+
+    # the same step as two calls (kv_store graph, then attn_decode_paged graph)
+    store_graphs = capture(lambda s: store_call(kvp, s), sets, stream)
+    dec_graphs = capture(lambda s: decode_call(kvp, s, w, ws), sets, stream)
+    ms_ustep, ms_decode, uwin = timed_loop(store_graphs, dec_graphs, args.steps, args.warmup, world)
+    assert kvp.device_status() == 0, "device status after the unfused decode loop"
+    ubps, ms_ustep = aggregate(step_bytes, ms_ustep, world)
+    dec_achieved = dec_b / (ms_decode * 1e-3) / 1e9
+    res["unfused"] = {"step": "kv_store graph + attn_decode_paged graph", "value": round(ubps / 1e9, 2),
+                      "unit": "GB/s", "ms_per_step": round(ms_ustep, 5), "steps": args.steps,
+                      "decode_call": {"kernel": "attn_decode_paged (split + merge)",
+                                      "achieved": round(dec_achieved, 1), "unit": "GB/s",
+                                      "frac": round(dec_achieved / peaks["hbm_gbs"], 4),
+                                      "algorithmic_bytes": dec_b, "ms_per_launch": round(ms_decode, 5)}}
+    res["uwindow"] = uwin
+    del store_graphs, dec_graphs
 
     # end to end through the API with host buffers (pinned), per step
     s0 = sets[0]
@@ -440,8 +493,7 @@ def measure_decode(args, kvp, W, dev, stream, world, peaks):
     def e2e_step():
         for hsrc, dst in zip(host_in, dev_in):
             dst.copy_(hsrc, non_blocking=True)
-        store_graphs[0].replay()
-        dec_graphs[0].replay()
+        app_graphs[0].replay()
         host_out.copy_(s0.out, non_blocking=True)
         stream.synchronize()
 
@@ -457,7 +509,7 @@ def measure_decode(args, kvp, W, dev, stream, world, peaks):
                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                   "how": "pinned host inputs copied in, graph replay, output copied out, stream sync each step"}
     res["footprint_gb"] = sum(2 * s.kc.numel() * 2 for s in sets) / 1e9
-    del store_graphs, dec_graphs, sets
+    del app_graphs, sets
     return res
 
 
@@ -572,7 +624,7 @@ def measure_bucketed(args, kvp, W, dev, stream, world, peaks):
             "line": {"workload": "decode B50 padded to the bucket-64 graph, 16/8/128 bs256 NB2048 "
                                  "ctx U[512,4096]", "value": round(bps / 1e9, 2), "unit": "GB/s",
                      "ms_per_step": round(ms, 4), "steps": steps,
-                     "step": "input copies into the graph buffers + replay (kv_store + attn_decode_paged)",
+                     "step": "input copies into the graph buffers + replay (attn_decode_paged_append)",
                      "frac_of_hbm": round(bps / 1e9 / peaks["hbm_gbs"], 4)}}
 
 
@@ -594,23 +646,23 @@ def measure_decode_large(args, kvp, W, dev, stream, world, peaks):
     m = w.steps[0].attn.meta
     ws = torch.empty(kvp.attn_decode_workspace_size(512, 32, 128, m.max_context_len, 256),
                      dtype=torch.uint8, device=dev)
-    sg = capture(lambda s_: store_call(kvp, s_), [ds], stream)
-    dg = capture(lambda s_: decode_call(kvp, s_, w, ws), [ds], stream)
+    ag = capture(lambda s_: append_call(kvp, s_, w, ws), [ds], stream)
     steps = max(10, min(100, args.steps // 100))
-    ms_step, ms_dec, win = timed_loop(sg, dg, steps, max(3, args.warmup // 4), world)
+    ms_step, ms_dec, win = timed_loop_single(ag, steps, max(3, args.warmup // 4), world)
     assert kvp.device_status() == 0, "device status after the large decode loop"
     bps, ms_step = aggregate(store_b + dec_b, ms_step, world)
-    achieved = dec_b / (ms_dec * 1e-3) / 1e9
-    del sg, dg, ds, ws
+    achieved = (store_b + dec_b) / (ms_dec * 1e-3) / 1e9
+    del ag, ds, ws
     torch.cuda.empty_cache()
     return {"window": win, "steps": steps,
             "line": {"workload": w.description, "value": round(bps / 1e9, 2), "unit": "GB/s",
                      "ms_per_step": round(ms_step, 4), "steps": steps,
-                     "step": "kv_store (512 new rows) + attn_decode_paged",
-                     "roofline": {"kernel": "attn_decode_paged (split + merge)", "bound": "hbm",
+                     "step": "attn_decode_paged_append (kv_store of 512 new rows fused)",
+                     "roofline": {"kernel": "attn_decode_paged_append (store + split + merge)",
+                                  "bound": "hbm",
                                   "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                   "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                                  "algorithmic_bytes": dec_b, "peak_source": peaks["source"],
+                                  "algorithmic_bytes": store_b + dec_b, "peak_source": peaks["source"],
                                   "ms_per_launch": round(ms_dec, 5)}}}
 
 
@@ -659,13 +711,13 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
         a.record()
         for layer in range(layers):
             kc, vc = kv[0, layer], kv[1, layer]
-            kvp.kv_store(k, v, slots, kc, vc)
             if pre:
+                kvp.kv_store(k, v, slots, kc, vc)
                 kvp.attn_prefill_varlen(q, cq, ck, m.max_seqlen_q, m.max_seqlen_k, k=k, v=v, k_cache=kc,
                                         v_cache=vc, block_tables=bt, num_kv_heads=hkv, softmax_scale=scale)
             else:
-                kvp.attn_decode_paged(q, kc, vc, bt, ctx, m.max_context_len, softmax_scale=scale,
-                                      workspace=ws)
+                kvp.attn_decode_paged_append(q, k, v, slots, kc, vc, bt, ctx, m.max_context_len,
+                                             softmax_scale=scale, workspace=ws)
         b.record()
         recs.append((pre, work * layers, a, b))
         sch.postprocess([(7 * i + n) % 151936 for i in ids])
@@ -681,7 +733,7 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
     torch.cuda.empty_cache()
     dec_gbs = dec_work / (dec_ms * 1e-3) / 1e9
     pre_tf = pre_work / (pre_ms * 1e-3) / 1e12
-    return {"window": (w0, w1), "launches": 2 * layers * len(recs) + layers * n_dec,
+    return {"window": (w0, w1), "launches": 2 * layers * len(recs),
             "line": {"workload": "engine trace: 256 requests, prompts/outputs U[100,1024], 28 layers "
                                  "16/8/128, bs 256, 768 blocks, native scheduler",
                      "steps": len(recs), "decode_steps": n_dec, "prefill_steps": len(recs) - n_dec,
@@ -690,7 +742,8 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
                                 "frac_of_hbm": round(dec_gbs / peaks["hbm_gbs"], 4)},
                      "prefill": {"value": round(pre_tf, 2), "unit": "TFLOP/s", "ms": round(pre_ms, 2),
                                  "frac_of_bf16_burst": round(pre_tf / peaks["bf16_tflops"], 4)},
-                     "how": "event pair around each step's 28 layers (store + attention); "
+                     "how": "event pair around each step's 28 layers (prefill: kv_store + "
+                            "attn_prefill_varlen; decode: attn_decode_paged_append); "
                             "inputs generated on the device before each step"}}
 
 
@@ -807,7 +860,7 @@ def run_ours(args, rank, world, local):
     dec = pre = None
     if args.only != "prefill":
         dec = measure_decode(args, kvp, W, dev, stream, world, peaks)
-        windows.append(dec["window"])
+        windows += [dec["window"], dec["uwindow"]]
     if args.only != "decode" and not args.no_prefill:
         pre = measure_prefill(args, kvp, W, dev, stream, world, peaks)
         windows.append(pre["window"])
@@ -851,19 +904,26 @@ def run_ours(args, rank, world, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dec["ms_step"], 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.description, "step": "kv_store (64 new rows) + attn_decode_paged",
+            "config": {"workload": w.description,
+                       "step": "attn_decode_paged_append: kv_store of the 64 new rows fused into the "
+                               "paged decode (split + merge)",
                        "global_batch": 64 * world, "parallelism": f"replicas x{world}",
                        "l2": f"{args.sets} input sets in rotation ({dec['footprint_gb']:.1f} GB of pools) vs 126 MB L2",
-                       "graph": "each step is two CUDA graph replays (store, attention)"},
+                       "graph": "each step is one CUDA graph replay"},
             "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
-            "gpu_launches": 3 * args.steps + (0 if pre is None else 2 * pre["line"]["steps"])
+            "unfused": dec["unfused"],
+            "gpu_launches": 2 * args.steps + 3 * args.steps
+                            + (0 if pre is None else 2 * pre["line"]["steps"])
                             + (0 if cb is None else cb["line"]["steps"])
                             + (0 if mx is None else 2 * mx["steps"])
-                            + (0 if bk is None else 3 * bk["steps"])
-                            + (0 if dl is None else 3 * dl["steps"])
+                            + (0 if bk is None else 2 * bk["steps"])
+                            + (0 if dl is None else 2 * dl["steps"])
                             + (0 if tr is None else tr["launches"]),
-            "gpu_launches_by_region": {"decode": {"kv_store": args.steps, "decode_split": args.steps,
+            "gpu_launches_by_region": {"decode": {"decode_split": args.steps,
                                                   "decode_merge": args.steps},
+                                       "decode_unfused": {"kv_store": args.steps,
+                                                          "decode_split": args.steps,
+                                                          "decode_merge": args.steps},
                                        "prefill": None if pre is None else
                                        {"kv_store": pre["line"]["steps"],
                                         "prefill": pre["line"]["steps"]},
@@ -873,11 +933,9 @@ def run_ours(args, rank, world, local):
                                        {"kv_store": mx["steps"], "prefill": mx["steps"]},
                                        "engine_trace": None if tr is None else {"all": tr["launches"]},
                                        "decode_b512": None if dl is None or not dl["steps"] else
-                                       {"kv_store": dl["steps"], "decode_split": dl["steps"],
-                                        "decode_merge": dl["steps"]},
+                                       {"decode_split": dl["steps"], "decode_merge": dl["steps"]},
                                        "decode_bucketed": None if bk is None else
-                                       {"kv_store": bk["steps"], "decode_split": bk["steps"],
-                                        "decode_merge": bk["steps"]}},
+                                       {"decode_split": bk["steps"], "decode_merge": bk["steps"]}},
             "clocks": clocks,
             "prefill": None if pre is None else pre["line"],
             "mixed": None if mx is None else mx["line"],

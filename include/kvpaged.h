@@ -8,6 +8,7 @@
  *   attn_prefill_varlen  varlen causal prefill over packed sequences, with a
  *                        prefix cache (only the uncached suffix is queried)
  *   attn_decode_paged    one query token per sequence over its paged history
+ *   attn_decode_paged_append  kv_store of the new rows + attn_decode_paged, fused
  *
  * Sources: "nano-vLLM-1" (Senjl's Digital Garden), ModelRunner sections
  * "3. KV cache 分配", "4. prefill 输入打包", "5. deocde 输入打包" and BlockManager
@@ -214,6 +215,45 @@ int attn_decode_paged(const kvp_bf16 *q, int64_t q_stride_tok, const kvp_bf16 *k
                       int num_heads, int num_kv_heads, int head_dim, float softmax_scale,
                       void *workspace, size_t workspace_bytes, kvp_bf16 *out,
                       int64_t out_stride_tok, kvp_stream_t stream);
+
+/*
+ * attn_decode_paged_append - kv_store of the step's new rows and
+ * attn_decode_paged in one launch.
+ *
+ * A decode step stores one new token per sequence (its K and V rows, at the
+ * slot of its last position) and then attends over the sequence's history
+ * including that token ("nano-vLLM-1" ModelRunner "5. deocde 输入打包":
+ * slot_mapping holds, per sequence, the slot of the token at position
+ * len - 1; context_lens counts that token).  This call computes exactly what
+ * kv_store(k, v, slot_mapping) followed by attn_decode_paged does, in one
+ * kernel launch (plus the merge launch): the new rows are written to the
+ * caches, and the sequence's last token is read from k / v instead of from
+ * the cache slot being written.
+ *
+ *   k, v            [num_seqs, num_kv_heads, head_dim] bf16, row strides
+ *                   k_stride_tok / v_stride_tok (multiples of 8 elements,
+ *                   16-byte aligned): the new row of sequence b is row b
+ *   slot_mapping    [num_seqs] int32: cache slot of sequence b's new row,
+ *                   -1 = no store (padding rows, context_lens 0)
+ *   k_cache/v_cache written at the slots of slot_mapping, read elsewhere
+ *   other arguments as attn_decode_paged
+ * Requirements beyond attn_decode_paged: for every b with context_lens[b]
+ * > 0 and slot_mapping[b] >= 0, slot_mapping[b] is the slot of position
+ * context_lens[b] - 1 through block_tables[b] (otherwise KVP_ERR_DEVICE_DATA
+ * is recorded in the device status; the row is still stored and the
+ * attention uses k / v for that position); no sequence of the batch reads
+ * another sequence's new-row slot (true for the engine, whose last blocks
+ * are private).  A slot >= num_blocks * block_size stores nothing and
+ * records KVP_ERR_DEVICE_DATA.
+ */
+int attn_decode_paged_append(const kvp_bf16 *q, int64_t q_stride_tok, const kvp_bf16 *k,
+                             const kvp_bf16 *v, int64_t k_stride_tok, int64_t v_stride_tok,
+                             const int32_t *slot_mapping, kvp_bf16 *k_cache, kvp_bf16 *v_cache,
+                             int64_t num_blocks, int block_size, const int32_t *block_tables,
+                             int max_blocks_per_seq, const int32_t *context_lens, int num_seqs,
+                             int max_context_len, int num_heads, int num_kv_heads, int head_dim,
+                             float softmax_scale, void *workspace, size_t workspace_bytes,
+                             kvp_bf16 *out, int64_t out_stride_tok, kvp_stream_t stream);
 
 /*
  * attn_decode_paged_noalloc - attn_decode_paged for callers that cannot

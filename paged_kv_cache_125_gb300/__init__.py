@@ -20,7 +20,7 @@ import os
 import threading
 
 __all__ = ["kv_store", "kv_copy_blocks", "attn_prefill_varlen", "attn_decode_paged", "attn_decode_workspace_size",
-           "attn_decode_paged_noalloc",
+           "attn_decode_paged_noalloc", "attn_decode_paged_append",
            "device_status", "library", "library_path", "KvpError"]
 
 _LIB_LOCK = threading.Lock()
@@ -46,6 +46,8 @@ SIGNATURES = {
                                  _I32, _F32, _P, _SZ, _P, _I64, _P]),
     "attn_decode_paged_noalloc": (_I32, [_P, _I64, _P, _P, _I64, _I32, _P, _I32, _P, _I32, _I32, _I32,
                                          _I32, _I32, _F32, _P, _I64, _P]),
+    "attn_decode_paged_append": (_I32, [_P, _I64, _P, _P, _I64, _I64, _P, _P, _P, _I64, _I32, _P, _I32,
+                                        _P, _I32, _I32, _I32, _I32, _I32, _F32, _P, _SZ, _P, _I64, _P]),
 }
 
 
@@ -200,6 +202,49 @@ def attn_decode_paged(q, k_cache, v_cache, block_tables, context_lens, max_conte
         block_tables.shape[1], _ptr(context_lens), b, int(max_context_len), hq, hkv, d, scale,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out), os_,
         _stream(k_cache)))
+    return out
+
+
+def attn_decode_paged_append(q, k, v, slot_mapping, k_cache, v_cache, block_tables, context_lens,
+                             max_context_len: int, softmax_scale: float | None = None, workspace=None,
+                             out=None):
+    """kv_store(k, v, slot_mapping, k_cache, v_cache) followed by
+    attn_decode_paged(q, ...), in one launch (see include/kvpaged.h).  Row b
+    of k / v is sequence b's new token, stored at slot_mapping[b] (the slot
+    of its position context_lens[b] - 1; -1 = padding row)."""
+    import torch
+    nb, bs, hkv, d = _cache_dims(k_cache, v_cache)
+    dev = k_cache.device
+    _require(q, "q", torch.bfloat16, 3, dev)
+    _require(k, "k", torch.bfloat16, 3, dev)
+    _require(v, "v", torch.bfloat16, 3, dev)
+    _require(slot_mapping, "slot_mapping", torch.int32, 1, dev)
+    b, hq = q.shape[0], q.shape[1]
+    qs = _rows(q, "q", hq, d)
+    ks, vs = _rows(k, "k", hkv, d), _rows(v, "v", hkv, d)
+    if k.shape[0] != b or v.shape[0] != b or slot_mapping.shape[0] != b:
+        raise ValueError("k, v and slot_mapping must have one row per sequence")
+    if not slot_mapping.is_contiguous():
+        raise ValueError("slot_mapping must be contiguous")
+    _require(block_tables, "block_tables", torch.int32, 2, dev)
+    _require(context_lens, "context_lens", torch.int32, 1, dev)
+    if block_tables.shape[0] != b or context_lens.shape[0] != b:
+        raise ValueError("block_tables / context_lens must have one row per sequence")
+    if not block_tables.is_contiguous() or not context_lens.is_contiguous():
+        raise ValueError("block_tables / context_lens must be contiguous")
+    if out is None:
+        out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=dev)
+    _require(out, "out", torch.bfloat16, 3, dev)
+    os_ = _rows(out, "out", hq, d)
+    need = attn_decode_workspace_size(b, hq, d, max_context_len, bs)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    _check(library().attn_decode_paged_append(
+        _ptr(q), qs, _ptr(k), _ptr(v), ks, vs, _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), nb,
+        bs, _ptr(block_tables), block_tables.shape[1], _ptr(context_lens), b, int(max_context_len),
+        hq, hkv, d, scale, _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(out),
+        os_, _stream(k_cache)))
     return out
 
 

@@ -193,6 +193,56 @@ int attn_decode_paged(const kvp_bf16* q, int64_t q_stride_tok, const kvp_bf16* k
   return KVP_OK;
 }
 
+int attn_decode_paged_append(const kvp_bf16* q, int64_t q_stride_tok, const kvp_bf16* k,
+                             const kvp_bf16* v, int64_t k_stride_tok, int64_t v_stride_tok,
+                             const int32_t* slot_mapping, kvp_bf16* k_cache, kvp_bf16* v_cache,
+                             int64_t num_blocks, int block_size, const int32_t* block_tables,
+                             int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                             int max_context_len, int num_heads, int num_kv_heads, int head_dim,
+                             float softmax_scale, void* workspace, size_t workspace_bytes,
+                             kvp_bf16* out, int64_t out_stride_tok, kvp_stream_t stream) {
+  if (num_seqs < 0 || max_context_len < 0 || num_blocks <= 0 || block_size <= 0 ||
+      max_blocks_per_seq < 0)
+    return fail(KVP_ERR_INVALID_ARG, "attn_decode_paged_append: bad sizes");
+  if (!kvp::decode_supported(num_heads, num_kv_heads, head_dim))
+    return fail(KVP_ERR_UNSUPPORTED,
+                "attn_decode_paged_append: unsupported heads %d/%d or head_dim %d", num_heads,
+                num_kv_heads, head_dim);
+  const int64_t row = (int64_t)num_kv_heads * head_dim;
+  if (q_stride_tok < (int64_t)num_heads * head_dim || out_stride_tok < (int64_t)num_heads * head_dim ||
+      k_stride_tok < row || v_stride_tok < row)
+    return fail(KVP_ERR_INVALID_ARG, "attn_decode_paged_append: row stride too small");
+  if ((int64_t)max_blocks_per_seq * block_size > (int64_t)1 << 30)
+    return fail(KVP_ERR_UNSUPPORTED, "attn_decode_paged_append: context capacity too large");
+  if (num_blocks * (int64_t)block_size >= ((int64_t)1 << 31))
+    return fail(KVP_ERR_UNSUPPORTED, "attn_decode_paged_append: pool has 2^31 or more slots");
+  if (num_seqs == 0) return KVP_OK;
+  if (!q || !k || !v || !slot_mapping || !k_cache || !v_cache || !block_tables || !context_lens ||
+      !out)
+    return fail(KVP_ERR_INVALID_ARG, "attn_decode_paged_append: null pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(out) || q_stride_tok % 8 || out_stride_tok % 8 ||
+      k_stride_tok % 8 || v_stride_tok % 8)
+    return fail(KVP_ERR_INVALID_ARG,
+                "attn_decode_paged_append: q, k, v, caches and out need 16-byte alignment and "
+                "row strides that are multiples of 8 elements");
+  int dev, *status, sms;
+  int rc = device_info(&dev, &status, &sms);
+  if (rc) return rc;
+  const kvp::DecodePlan plan = kvp::plan_decode(num_seqs, num_heads, head_dim, max_context_len, sms);
+  if (!workspace || workspace_bytes < plan.total_bytes || !aligned16(workspace))
+    return fail(KVP_ERR_WORKSPACE, "attn_decode_paged_append: workspace needs %zu bytes (got %zu)",
+                plan.total_bytes, workspace_bytes);
+  const kvp::DecodeAppend app{k, v, k_stride_tok, v_stride_tok, slot_mapping, k_cache, v_cache};
+  cudaError_t e = kvp::launch_decode(q, q_stride_tok, k_cache, v_cache, num_blocks, block_size,
+                                     block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                                     num_heads, num_kv_heads, head_dim, softmax_scale, plan,
+                                     workspace, out, out_stride_tok, status, (cudaStream_t)stream,
+                                     &app);
+  if (e != cudaSuccess) return fail_cuda(e, "attn_decode_paged_append launch");
+  return KVP_OK;
+}
+
 int attn_prefill_varlen(const kvp_bf16* q, int64_t q_stride_tok, int64_t total_q,
                         const kvp_bf16* k, const kvp_bf16* v, int64_t kv_stride_tok,
                         int64_t total_k, const kvp_bf16* k_cache,

@@ -27,6 +27,13 @@
 //   fp32 dot product over the lane's slice reduced over 8 lanes by shuffles,
 //   with q pre-scaled by softmax_scale * log2(e) so the softmax uses exp2.
 //   The running max is warp-uniform and updated once per stage.
+// * Optional store of the step's new rows (attn_decode_paged_append): the
+//   kv_store of one new token per sequence is folded into the same launch.
+//   CTA i writes the rows of sequences i, i + P, ... into the cache slots
+//   slot_mapping[b]; the stage that ends at a sequence's last context token
+//   takes that token's K and V row straight from the new rows (one more bulk
+//   copy) instead of from the cache, so no CTA reads a slot written in the
+//   same launch.
 #include <cfloat>
 
 #include "kvp_device.cuh"
@@ -88,6 +95,13 @@ struct DecodeArgs {
   uint16_t* out;
   int64_t out_stride;
   int* status;
+  // Fused store of the new rows (null k_new: plain decode).
+  const uint16_t* k_new;  // [num_seqs, Hkv, D], row stride k_new_stride
+  const uint16_t* v_new;
+  int64_t k_new_stride, v_new_stride;
+  const int32_t* slot_mapping;  // [num_seqs]; -1 = no store
+  uint16_t* k_cache_w;          // the caches, written by the store
+  uint16_t* v_cache_w;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -122,11 +136,136 @@ __host__ __device__ constexpr size_t decode_smem_bytes() {
 
 // ---------------------------------------------------------------- producer
 
+// Stage loop of the producer (one thread): copies the CTA's token range
+// [start, end), first sequence b0 starting at token cum0 of the batch, into
+// the ring, then posts the end marker.
+template <int D>
+__device__ void stream_stages(const DecodeArgs& a, uint8_t* ringK, uint8_t* ringV, StageMeta* meta,
+                              uint64_t* full, uint64_t* empty, long long start, long long end,
+                              int b0, long long cum0, int cap) {
+  const int Hkv = a.num_kv_heads;
+  a.split_seq[blockIdx.x] = -1;
+  const int T = kTokensAllHeads / Hkv;
+  const int64_t row_elems = (int64_t)Hkv * D;
+  int s = 0;
+  uint32_t ph = 0;
+  uint32_t issued = 0, issued_ph = 0;  // per stage: ever issued / parity of the last issue
+  bool ok = true;
+
+  long long pos = start, cum = cum0;
+  int b = b0;
+  while (ok && pos < end && b < a.num_seqs) {
+    const int L = clamp_len(a.ctx[b], cap);
+    if (L == 0) {
+      ++b;
+      continue;
+    }
+    const long long seq_end = cum + L;
+    const long long seg_end = end < seq_end ? end : seq_end;
+    int t = (int)(pos - cum);
+    const int t1 = (int)(seg_end - cum);
+    const int seg_flags = (pos > cum ? F_ENTERED : 0) | (seg_end < seq_end ? F_EXITS : 0);
+    bool first = true;
+    int cur_bi = -1, phys = 0;
+    while (t < t1) {
+      const int bi = t / a.block_size, off = t - bi * a.block_size;
+      int n = a.block_size - off;
+      if (n > T) n = T;
+      if (n > t1 - t) n = t1 - t;
+      if (bi != cur_bi) {
+        cur_bi = bi;
+        phys = a.block_tables[(int64_t)b * a.max_blocks + bi];
+        if (phys < 0 || phys >= a.num_blocks) {
+          record_error(a.status, KVP_ERR_DEVICE_DATA);
+          phys = 0;  // never dereference an out-of-range block
+        }
+      }
+      if (!mbar_wait(&empty[s], ph ^ 1u, a.status)) {
+        ok = false;
+        break;
+      }
+      meta[s].b = b;
+      meta[s].n = n;
+      meta[s].flags = (first ? F_NEW : 0) | (t + n == t1 ? F_LAST : 0) | seg_flags;
+      const uint32_t bytes = (uint32_t)(n * row_elems * sizeof(uint16_t));
+      mbar_arrive_expect_tx(&full[s], 2 * bytes);
+      const int64_t row0 = ((int64_t)phys * a.block_size + off) * row_elems;
+      uint8_t* dk = ringK + (size_t)s * stage_half_bytes<D>();
+      uint8_t* dv = ringV + (size_t)s * stage_half_bytes<D>();
+      // With the fused store, the sequence's last token comes from the new rows.
+      const bool tail = a.k_new != nullptr && t + n == L;
+      const uint32_t row_bytes = (uint32_t)(row_elems * sizeof(uint16_t));
+      const uint32_t cbytes = tail ? bytes - row_bytes : bytes;
+      if (cbytes) {
+        bulk_g2s(dk, a.k_cache + row0, cbytes, &full[s]);
+        bulk_g2s(dv, a.v_cache + row0, cbytes, &full[s]);
+      }
+      if (tail) {
+        bulk_g2s(dk + cbytes, a.k_new + (int64_t)b * a.k_new_stride, row_bytes, &full[s]);
+        bulk_g2s(dv + cbytes, a.v_new + (int64_t)b * a.v_new_stride, row_bytes, &full[s]);
+      }
+      issued |= 1u << s;
+      issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
+      first = false;
+      t += n;
+      if (++s == kStages) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    if (seg_flags & F_EXITS) a.split_seq[blockIdx.x] = b;
+    pos = seg_end;
+    cum = seq_end;
+    ++b;
+  }
+  if (ok && mbar_wait(&empty[s], ph ^ 1u, a.status)) {
+    meta[s].flags = F_DONE;
+    mbar_arrive(&full[s]);
+    return;
+  }
+  // A wait expired: let every copy this CTA issued land before the CTA exits.
+  for (int i = 0; i < kStages; ++i)
+    if (issued >> i & 1u) mbar_wait(&full[i], issued_ph >> i & 1u, a.status);
+}
+
+// Store of the step's new rows (attn_decode_paged_append), one warp: this CTA
+// writes the rows of sequences blockIdx.x + k * gridDim.x.  The slot must be
+// that of the sequence's last context token (the engine's decode step);
+// otherwise the step would not equal store-then-attend, and the mismatch is
+// reported.
+template <int D>
+__device__ void fused_store(const DecodeArgs& a, int lane, int cap) {
+  const int64_t row_elems = (int64_t)a.num_kv_heads * D;
+  const int64_t pool_slots = a.num_blocks * a.block_size;
+  for (int b = blockIdx.x; b < a.num_seqs; b += gridDim.x) {
+    const int slot = a.slot_mapping[b];
+    if (slot < 0) continue;
+    if (slot >= pool_slots) {
+      if (lane == 0) record_error(a.status, KVP_ERR_DEVICE_DATA);
+      continue;
+    }
+    const int L = clamp_len(a.ctx[b], cap);
+    if (L > 0 && lane == 0) {
+      const int lb = (L - 1) / a.block_size;
+      const int phys = a.block_tables[(int64_t)b * a.max_blocks + lb];
+      if ((int64_t)phys * a.block_size + (L - 1 - lb * a.block_size) != slot)
+        record_error(a.status, KVP_ERR_DEVICE_DATA);
+    }
+    const uint4* ks = reinterpret_cast<const uint4*>(a.k_new + (int64_t)b * a.k_new_stride);
+    const uint4* vs = reinterpret_cast<const uint4*>(a.v_new + (int64_t)b * a.v_new_stride);
+    uint4* kd = reinterpret_cast<uint4*>(a.k_cache_w + (int64_t)slot * row_elems);
+    uint4* vd = reinterpret_cast<uint4*>(a.v_cache_w + (int64_t)slot * row_elems);
+    for (int i = lane; i < row_elems / 8; i += 32) {
+      kd[i] = ks[i];
+      vd[i] = vs[i];
+    }
+  }
+}
+
 template <int D>
 __device__ void decode_producer(const DecodeArgs& a, uint8_t* ringK, uint8_t* ringV,
                                 StageMeta* meta, uint64_t* full, uint64_t* empty) {
   const int lane = threadIdx.x & 31;
-  const int Hkv = a.num_kv_heads;
   const int cap = a.max_blocks * a.block_size;
   const int P = gridDim.x;
 
@@ -174,78 +313,12 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* ringK, uint8_t* ri
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
-  if (lane != 0) return;
-
-  a.split_seq[blockIdx.x] = -1;
-  const int T = kTokensAllHeads / Hkv;
-  const int64_t row_elems = (int64_t)Hkv * D;
-  int s = 0;
-  uint32_t ph = 0;
-  uint32_t issued = 0, issued_ph = 0;  // per stage: ever issued / parity of the last issue
-  bool ok = true;
-
-  long long pos = start, cum = cum0;
-  int b = b0;
-  while (ok && pos < end && b < a.num_seqs) {
-    const int L = clamp_len(a.ctx[b], cap);
-    if (L == 0) {
-      ++b;
-      continue;
-    }
-    const long long seq_end = cum + L;
-    const long long seg_end = end < seq_end ? end : seq_end;
-    int t = (int)(pos - cum);
-    const int t1 = (int)(seg_end - cum);
-    const int seg_flags = (pos > cum ? F_ENTERED : 0) | (seg_end < seq_end ? F_EXITS : 0);
-    bool first = true;
-    int cur_bi = -1, phys = 0;
-    while (t < t1) {
-      const int bi = t / a.block_size, off = t - bi * a.block_size;
-      int n = a.block_size - off;
-      if (n > T) n = T;
-      if (n > t1 - t) n = t1 - t;
-      if (bi != cur_bi) {
-        cur_bi = bi;
-        phys = a.block_tables[(int64_t)b * a.max_blocks + bi];
-        if (phys < 0 || phys >= a.num_blocks) {
-          record_error(a.status, KVP_ERR_DEVICE_DATA);
-          phys = 0;  // never dereference an out-of-range block
-        }
-      }
-      if (!mbar_wait(&empty[s], ph ^ 1u, a.status)) {
-        ok = false;
-        break;
-      }
-      meta[s].b = b;
-      meta[s].n = n;
-      meta[s].flags = (first ? F_NEW : 0) | (t + n == t1 ? F_LAST : 0) | seg_flags;
-      const uint32_t bytes = (uint32_t)(n * row_elems * sizeof(uint16_t));
-      mbar_arrive_expect_tx(&full[s], 2 * bytes);
-      const int64_t row0 = ((int64_t)phys * a.block_size + off) * row_elems;
-      bulk_g2s(ringK + (size_t)s * stage_half_bytes<D>(), a.k_cache + row0, bytes, &full[s]);
-      bulk_g2s(ringV + (size_t)s * stage_half_bytes<D>(), a.v_cache + row0, bytes, &full[s]);
-      issued |= 1u << s;
-      issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
-      first = false;
-      t += n;
-      if (++s == kStages) {
-        s = 0;
-        ph ^= 1u;
-      }
-    }
-    if (seg_flags & F_EXITS) a.split_seq[blockIdx.x] = b;
-    pos = seg_end;
-    cum = seq_end;
-    ++b;
-  }
-  if (ok && mbar_wait(&empty[s], ph ^ 1u, a.status)) {
-    meta[s].flags = F_DONE;
-    mbar_arrive(&full[s]);
-    return;
-  }
-  // A wait expired: let every copy this CTA issued land before the CTA exits.
-  for (int i = 0; i < kStages; ++i)
-    if (issued >> i & 1u) mbar_wait(&full[i], issued_ph >> i & 1u, a.status);
+  if (lane == 0)
+    stream_stages<D>(a, ringK, ringV, meta, full, empty, start, end, b0, cum0, cap);
+  // The fused store, by the whole warp once every stage is issued: it overlaps
+  // the consumers' last stages instead of delaying the first copies.
+  __syncwarp();
+  if (a.k_new != nullptr) fused_store<D>(a, lane, cap);
 }
 
 // ---------------------------------------------------------------- consumers
@@ -648,8 +721,16 @@ cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k
                           const int32_t* block_tables, int max_blocks, const int32_t* ctx,
                           int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                           float softmax_scale, const DecodePlan& plan, void* workspace,
-                          uint16_t* out, int64_t out_stride, int* status, cudaStream_t stream) {
+                          uint16_t* out, int64_t out_stride, int* status, cudaStream_t stream,
+                          const DecodeAppend* app) {
   DecodeArgs a;
+  a.k_new = app ? app->k : nullptr;
+  a.v_new = app ? app->v : nullptr;
+  a.k_new_stride = app ? app->k_stride : 0;
+  a.v_new_stride = app ? app->v_stride : 0;
+  a.slot_mapping = app ? app->slot_mapping : nullptr;
+  a.k_cache_w = app ? app->k_cache : nullptr;
+  a.v_cache_w = app ? app->v_cache : nullptr;
   a.q = q;
   a.q_stride = q_stride;
   a.k_cache = k_cache;

@@ -35,12 +35,22 @@ struct DecodePlan {
 DecodePlan plan_decode(int num_seqs, int num_heads, int head_dim, int max_context_len,
                        int num_sms);
 bool decode_supported(int num_heads, int num_kv_heads, int head_dim);
+// New rows of a fused store (attn_decode_paged_append).
+struct DecodeAppend {
+  const uint16_t* k;
+  const uint16_t* v;
+  int64_t k_stride, v_stride;
+  const int32_t* slot_mapping;
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+};
 cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k_cache,
                           const uint16_t* v_cache, int64_t num_blocks, int block_size,
                           const int32_t* block_tables, int max_blocks, const int32_t* ctx,
                           int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                           float softmax_scale, const DecodePlan& plan, void* workspace,
-                          uint16_t* out, int64_t out_stride, int* status, cudaStream_t stream);
+                          uint16_t* out, int64_t out_stride, int* status, cudaStream_t stream,
+                          const DecodeAppend* app = nullptr);
 
 // prefill.cu
 bool prefill_supported(int num_heads, int num_kv_heads, int head_dim, int block_size);

@@ -4,15 +4,16 @@ decode steps ("nano-vLLM-1", ModelRunner: graphs captured for batch sizes
 graph of the smallest bucket >= b after copying its inputs into the graph's
 fixed buffers; the unused rows are padding: slot_mapping -1, context_lens 0).
 
-Every launch in a captured graph is a library call (``kv_store`` then
-``attn_decode_paged``); the launch configuration depends only on the bucket
+Every launch in a captured graph is a library call
+(``attn_decode_paged_append``: the store of the new rows fused into the
+paged decode); the launch configuration depends only on the bucket
 and the fixed capacities, never on the step's data, so one capture serves
 every step.  Padding rows write nothing (slot -1) and read nothing (context
 0), and their output rows are zero.
 """
 from __future__ import annotations
 
-from . import attn_decode_paged, attn_decode_workspace_size, kv_store
+from . import attn_decode_paged_append, attn_decode_workspace_size
 
 
 def default_buckets(max_bs: int) -> list[int]:
@@ -69,10 +70,10 @@ class DecodeGraphs:
             self.graphs[b] = self._capture(b)
 
     def _step(self, b: int) -> None:
-        kv_store(self.k[:b], self.v[:b], self.slots[:b], self.k_cache, self.v_cache)
-        attn_decode_paged(self.q[:b], self.k_cache, self.v_cache, self.block_tables[:b],
-                          self.context_lens[:b], self.capacity, softmax_scale=self.scale,
-                          workspace=self.workspace, out=self.out[:b])
+        attn_decode_paged_append(self.q[:b], self.k[:b], self.v[:b], self.slots[:b], self.k_cache,
+                                 self.v_cache, self.block_tables[:b], self.context_lens[:b],
+                                 self.capacity, softmax_scale=self.scale, workspace=self.workspace,
+                                 out=self.out[:b])
 
     def _capture(self, b: int):
         import torch

@@ -63,17 +63,25 @@ def gpu_pool(w: W.Workload, device="cuda"):
     return kc, vc
 
 
-def run_gpu(w: W.Workload, device="cuda"):
-    """-> (per-step bf16 outputs on the device, k_cache, v_cache)."""
+def run_gpu(w: W.Workload, device="cuda", fused_decode=False):
+    """-> (per-step bf16 outputs on the device, k_cache, v_cache).  With
+    fused_decode, decode steps go through attn_decode_paged_append (store and
+    attention in one launch) instead of kv_store + attn_decode_paged."""
     kc, vc = gpu_pool(w, device)
     for st in w.setup:
         kvp.kv_store(st.k.to(device), st.v.to(device), st.slot_mapping.to(device), kc, vc)
     outs = []
     for step in w.steps:
         s = step.store
-        kvp.kv_store(s.k.to(device), s.v.to(device), s.slot_mapping.to(device), kc, vc)
         a = step.attn
         m = a.meta
+        if fused_decode and not step.is_prefill:
+            outs.append(kvp.attn_decode_paged_append(
+                a.q.to(device), s.k.to(device), s.v.to(device), s.slot_mapping.to(device), kc, vc,
+                m.block_tables.to(device), m.context_lens.to(device), m.max_context_len,
+                softmax_scale=w.scale))
+            continue
+        kvp.kv_store(s.k.to(device), s.v.to(device), s.slot_mapping.to(device), kc, vc)
         if step.is_prefill:
             bt = None if m.block_tables is None else m.block_tables.to(device)
             o = kvp.attn_prefill_varlen(a.q.to(device), m.cu_seqlens_q.to(device), m.cu_seqlens_k.to(device),

@@ -82,8 +82,8 @@ def test_kv_store_out_of_range_slot_is_skipped_and_flagged():
 
 # --------------------------------------------------------------------------- decode
 
-def _check_decode_workload(w, seqs=None):
-    outs, kc, vc = run_gpu(w)
+def _check_decode_workload(w, seqs=None, fused=False):
+    outs, kc, vc = run_gpu(w, fused_decode=fused)
     ref, kr, vr = run_oracle(w, seqs_for=(lambda i: seqs) if seqs is not None else None)
     assert np.array_equal(u16(kc), kr) and np.array_equal(u16(vc), vr), "cache differs after kv_store"
     mask = None if seqs is None else np.asarray(seqs)
@@ -192,3 +192,73 @@ def test_decode_config4_full_pool_sampled():
     ref = oracle.decode(w.steps[0].attn.q[sample].cpu(), kh, vh, W.prepare_block_tables(tables),
                         torch.tensor(ctxs, dtype=torch.int32), 32, 8, w.scale)
     assert_attn_close(outs[0][sample], ref, "config4 sample")
+
+
+# --------------------------------------------------------------------------- fused store + decode
+
+def test_decode_append_config2_full_size():
+    """attn_decode_paged_append on the 64-sequence step: the cache after the
+    call is bit-exact (store), the outputs match the oracle's store-then-decode."""
+    _check_decode_workload(W.config2_decode(), fused=True)
+
+
+@pytest.mark.parametrize("hq,hkv,d,bs,lens", [
+    (2, 1, 64, 16, [1, 16, 17, 300, 33]),
+    (8, 8, 128, 256, [5000, 1, 256, 257, 700]),
+    (32, 8, 128, 256, [8192, 128, 4096]),
+    (4, 2, 128, 48, [47, 48, 49, 2000]),
+    (8, 1, 64, 64, [1000]),
+])
+def test_decode_append_shapes_and_ragged_lengths(hq, hkv, d, bs, lens):
+    """New rows at the first slot of a block (stage of one token), mid-block and
+    at a block's last slot; group sizes 1..8."""
+    nb = sum(W.num_blocks_for(L, bs) for L in lens) + 7
+    w = W.decode_workload(f"append_{hq}_{hkv}_{d}_{bs}", lens, hq, hkv, d, bs, nb)
+    _check_decode_workload(w, fused=True)
+
+
+def test_decode_append_long_sequence_crosses_every_cta():
+    """The new token lands in the last CTA's chunk of a sequence split over all
+    CTAs; the others read only stored history."""
+    w = W.decode_workload("append_long", [65536, 3], 16, 8, 128, 256, 300)
+    _check_decode_workload(w, fused=True)
+
+
+def test_decode_append_padding_rows():
+    """Rows with slot -1 and context 0 (the graph path's padding) store nothing
+    and produce zeros; the other rows are unaffected."""
+    w = W.decode_workload("append_pad", [100, 1, 700], 4, 2, 128, 16, 64)
+    step = w.steps[0]
+    kc, vc = gpu_pool(w)
+    m, st = step.attn.meta, step.store
+    ctx, slots = m.context_lens.clone(), st.slot_mapping.clone()
+    ctx[1], slots[1] = 0, -1
+    before = u16(kc).copy()
+    out = kvp.attn_decode_paged_append(step.attn.q.cuda(), st.k.cuda(), st.v.cuda(), slots.cuda(), kc,
+                                       vc, m.block_tables.cuda(), ctx.cuda(), m.max_context_len,
+                                       softmax_scale=w.scale)
+    torch.cuda.synchronize()
+    assert out[1].float().abs().max().item() == 0.0
+    kr, vr = oracle_pool(w)
+    oracle.kv_store(st.k, st.v, slots, kr, vr)
+    assert np.array_equal(u16(kc), kr) and np.array_equal(u16(vc), vr)
+    changed = np.argwhere((u16(kc) != before).any(axis=(2, 3)))
+    assert len(changed) == 2  # the two stored rows only
+    ref = oracle.decode(step.attn.q, kr, vr, m.block_tables, ctx, 4, 2, w.scale)
+    assert_attn_close(out, ref, "append with padding rows")
+
+
+def test_decode_append_slot_mismatch_is_flagged():
+    """A slot that is not the one of position context_len - 1 is reported
+    (KVP_ERR_DEVICE_DATA); the row is still stored there."""
+    w = W.decode_workload("append_bad_slot", [40, 40], 4, 2, 64, 16, 16)
+    step = w.steps[0]
+    kc, vc = gpu_pool(w)
+    m, st = step.attn.meta, step.store
+    slots = st.slot_mapping.clone()
+    slots[0] = int(slots[0]) - 1  # an earlier slot of the same block
+    kvp.attn_decode_paged_append(step.attn.q.cuda(), st.k.cuda(), st.v.cuda(), slots.cuda(), kc, vc,
+                                 m.block_tables.cuda(), m.context_lens.cuda(), m.max_context_len)
+    assert kvp.device_status() == -6
+    flat = kc.view(-1, 2, 64)
+    assert torch.equal(flat[int(slots[0])].cpu().view(torch.int16), st.k[0].view(torch.int16))
