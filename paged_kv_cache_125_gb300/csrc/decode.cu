@@ -95,7 +95,12 @@ struct DecodeArgs {
   uint16_t* out;
   int64_t out_stride;
   int* status;
-  // Fused store of the new rows (null k_new: plain decode).
+};
+
+// Fused store of the new rows (null k_new: plain decode).  A kernel parameter
+// of its own: the consumer warps never touch it, and keeping it out of
+// DecodeArgs keeps their register allocation as it is without it.
+struct AppendArgs {
   const uint16_t* k_new;  // [num_seqs, Hkv, D], row stride k_new_stride
   const uint16_t* v_new;
   int64_t k_new_stride, v_new_stride;
@@ -140,9 +145,9 @@ __host__ __device__ constexpr size_t decode_smem_bytes() {
 // [start, end), first sequence b0 starting at token cum0 of the batch, into
 // the ring, then posts the end marker.
 template <int D>
-__device__ void stream_stages(const DecodeArgs& a, uint8_t* ringK, uint8_t* ringV, StageMeta* meta,
-                              uint64_t* full, uint64_t* empty, long long start, long long end,
-                              int b0, long long cum0, int cap) {
+__device__ void stream_stages(const DecodeArgs& a, const AppendArgs& app, uint8_t* ringK,
+                              uint8_t* ringV, StageMeta* meta, uint64_t* full, uint64_t* empty,
+                              long long start, long long end, int b0, long long cum0, int cap) {
   const int Hkv = a.num_kv_heads;
   a.split_seq[blockIdx.x] = -1;
   const int T = kTokensAllHeads / Hkv;
@@ -193,7 +198,7 @@ __device__ void stream_stages(const DecodeArgs& a, uint8_t* ringK, uint8_t* ring
       uint8_t* dk = ringK + (size_t)s * stage_half_bytes<D>();
       uint8_t* dv = ringV + (size_t)s * stage_half_bytes<D>();
       // With the fused store, the sequence's last token comes from the new rows.
-      const bool tail = a.k_new != nullptr && t + n == L;
+      const bool tail = app.k_new != nullptr && t + n == L;
       const uint32_t row_bytes = (uint32_t)(row_elems * sizeof(uint16_t));
       const uint32_t cbytes = tail ? bytes - row_bytes : bytes;
       if (cbytes) {
@@ -201,8 +206,8 @@ __device__ void stream_stages(const DecodeArgs& a, uint8_t* ringK, uint8_t* ring
         bulk_g2s(dv, a.v_cache + row0, cbytes, &full[s]);
       }
       if (tail) {
-        bulk_g2s(dk + cbytes, a.k_new + (int64_t)b * a.k_new_stride, row_bytes, &full[s]);
-        bulk_g2s(dv + cbytes, a.v_new + (int64_t)b * a.v_new_stride, row_bytes, &full[s]);
+        bulk_g2s(dk + cbytes, app.k_new + (int64_t)b * app.k_new_stride, row_bytes, &full[s]);
+        bulk_g2s(dv + cbytes, app.v_new + (int64_t)b * app.v_new_stride, row_bytes, &full[s]);
       }
       issued |= 1u << s;
       issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
@@ -234,11 +239,11 @@ __device__ void stream_stages(const DecodeArgs& a, uint8_t* ringK, uint8_t* ring
 // otherwise the step would not equal store-then-attend, and the mismatch is
 // reported.
 template <int D>
-__device__ void fused_store(const DecodeArgs& a, int lane, int cap) {
+__device__ void fused_store(const DecodeArgs& a, const AppendArgs& app, int lane, int cap) {
   const int64_t row_elems = (int64_t)a.num_kv_heads * D;
   const int64_t pool_slots = a.num_blocks * a.block_size;
   for (int b = blockIdx.x; b < a.num_seqs; b += gridDim.x) {
-    const int slot = a.slot_mapping[b];
+    const int slot = app.slot_mapping[b];
     if (slot < 0) continue;
     if (slot >= pool_slots) {
       if (lane == 0) record_error(a.status, KVP_ERR_DEVICE_DATA);
@@ -251,10 +256,10 @@ __device__ void fused_store(const DecodeArgs& a, int lane, int cap) {
       if ((int64_t)phys * a.block_size + (L - 1 - lb * a.block_size) != slot)
         record_error(a.status, KVP_ERR_DEVICE_DATA);
     }
-    const uint4* ks = reinterpret_cast<const uint4*>(a.k_new + (int64_t)b * a.k_new_stride);
-    const uint4* vs = reinterpret_cast<const uint4*>(a.v_new + (int64_t)b * a.v_new_stride);
-    uint4* kd = reinterpret_cast<uint4*>(a.k_cache_w + (int64_t)slot * row_elems);
-    uint4* vd = reinterpret_cast<uint4*>(a.v_cache_w + (int64_t)slot * row_elems);
+    const uint4* ks = reinterpret_cast<const uint4*>(app.k_new + (int64_t)b * app.k_new_stride);
+    const uint4* vs = reinterpret_cast<const uint4*>(app.v_new + (int64_t)b * app.v_new_stride);
+    uint4* kd = reinterpret_cast<uint4*>(app.k_cache_w + (int64_t)slot * row_elems);
+    uint4* vd = reinterpret_cast<uint4*>(app.v_cache_w + (int64_t)slot * row_elems);
     for (int i = lane; i < row_elems / 8; i += 32) {
       kd[i] = ks[i];
       vd[i] = vs[i];
@@ -263,8 +268,8 @@ __device__ void fused_store(const DecodeArgs& a, int lane, int cap) {
 }
 
 template <int D>
-__device__ void decode_producer(const DecodeArgs& a, uint8_t* ringK, uint8_t* ringV,
-                                StageMeta* meta, uint64_t* full, uint64_t* empty) {
+__device__ void decode_producer(const DecodeArgs& a, const AppendArgs& app, uint8_t* ringK,
+                                uint8_t* ringV, StageMeta* meta, uint64_t* full, uint64_t* empty) {
   const int lane = threadIdx.x & 31;
   const int cap = a.max_blocks * a.block_size;
   const int P = gridDim.x;
@@ -314,11 +319,11 @@ __device__ void decode_producer(const DecodeArgs& a, uint8_t* ringK, uint8_t* ri
     }
   }
   if (lane == 0)
-    stream_stages<D>(a, ringK, ringV, meta, full, empty, start, end, b0, cum0, cap);
+    stream_stages<D>(a, app, ringK, ringV, meta, full, empty, start, end, b0, cum0, cap);
   // The fused store, by the whole warp once every stage is issued: it overlaps
   // the consumers' last stages instead of delaying the first copies.
   __syncwarp();
-  if (a.k_new != nullptr) fused_store<D>(a, lane, cap);
+  if (app.k_new != nullptr) fused_store<D>(a, app, lane, cap);
 }
 
 // ---------------------------------------------------------------- consumers
@@ -598,7 +603,8 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
 }
 
 template <int D, int G, int HS>
-__global__ void __maxnreg__(HS == 1 ? 168 : 96) decode_split_kernel(const DecodeArgs a) {
+__global__ void __maxnreg__(HS == 1 ? 168 : 96) decode_split_kernel(const DecodeArgs a,
+                                                                const AppendArgs app) {
   constexpr int CW = consumer_warps<HS>(), GE = G / HS;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ringK = smem;
@@ -627,7 +633,7 @@ __global__ void __maxnreg__(HS == 1 ? 168 : 96) decode_split_kernel(const Decode
   }
   __syncthreads();
   if ((threadIdx.x >> 5) == CW)
-    decode_producer<D>(a, ringK, ringV, meta, full, empty);
+    decode_producer<D>(a, app, ringK, ringV, meta, full, empty);
   else
     decode_consumer<D, GE, HS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
 }
@@ -667,13 +673,14 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const float* __restrict
 }
 
 template <int D, int G>
-cudaError_t launch_decode_t(const DecodeArgs& a, int ctas, cudaStream_t stream) {
+cudaError_t launch_decode_t(const DecodeArgs& a, const AppendArgs& app, int ctas,
+                            cudaStream_t stream) {
   constexpr int HS = head_split<D, G>();
   const size_t smem = decode_smem_bytes<D, G>();
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, HS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_split_kernel<D, G, HS><<<ctas, (consumer_warps<HS>() + 1) * 32, smem, stream>>>(a);
+  decode_split_kernel<D, G, HS><<<ctas, (consumer_warps<HS>() + 1) * 32, smem, stream>>>(a, app);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -724,13 +731,16 @@ cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k
                           uint16_t* out, int64_t out_stride, int* status, cudaStream_t stream,
                           const DecodeAppend* app) {
   DecodeArgs a;
-  a.k_new = app ? app->k : nullptr;
-  a.v_new = app ? app->v : nullptr;
-  a.k_new_stride = app ? app->k_stride : 0;
-  a.v_new_stride = app ? app->v_stride : 0;
-  a.slot_mapping = app ? app->slot_mapping : nullptr;
-  a.k_cache_w = app ? app->k_cache : nullptr;
-  a.v_cache_w = app ? app->v_cache : nullptr;
+  AppendArgs ap{};
+  if (app) {
+    ap.k_new = app->k;
+    ap.v_new = app->v;
+    ap.k_new_stride = app->k_stride;
+    ap.v_new_stride = app->v_stride;
+    ap.slot_mapping = app->slot_mapping;
+    ap.k_cache_w = app->k_cache;
+    ap.v_cache_w = app->v_cache;
+  }
   a.q = q;
   a.q_stride = q_stride;
   a.k_cache = k_cache;
@@ -753,16 +763,16 @@ cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k
   const int G = num_heads / num_kv_heads;
   if (head_dim == 128) {
     switch (G) {
-      case 1: return launch_decode_t<128, 1>(a, plan.ctas, stream);
-      case 2: return launch_decode_t<128, 2>(a, plan.ctas, stream);
-      case 4: return launch_decode_t<128, 4>(a, plan.ctas, stream);
+      case 1: return launch_decode_t<128, 1>(a, ap, plan.ctas, stream);
+      case 2: return launch_decode_t<128, 2>(a, ap, plan.ctas, stream);
+      case 4: return launch_decode_t<128, 4>(a, ap, plan.ctas, stream);
     }
   } else if (head_dim == 64) {
     switch (G) {
-      case 1: return launch_decode_t<64, 1>(a, plan.ctas, stream);
-      case 2: return launch_decode_t<64, 2>(a, plan.ctas, stream);
-      case 4: return launch_decode_t<64, 4>(a, plan.ctas, stream);
-      case 8: return launch_decode_t<64, 8>(a, plan.ctas, stream);
+      case 1: return launch_decode_t<64, 1>(a, ap, plan.ctas, stream);
+      case 2: return launch_decode_t<64, 2>(a, ap, plan.ctas, stream);
+      case 4: return launch_decode_t<64, 4>(a, ap, plan.ctas, stream);
+      case 8: return launch_decode_t<64, 8>(a, ap, plan.ctas, stream);
     }
   }
   return cudaErrorInvalidValue;
