@@ -60,6 +60,19 @@ __host__ __device__ constexpr int consumer_warps() {
 }
 constexpr int kTokensAllHeads = 64;  // tokens * kv heads per stage
 
+// With the head split the producer gets a warpgroup of its own (warps CW ..
+// CW + 3; only the first works) so that setmaxnreg can move registers from it
+// to the consumers: the launch gives 20 warps x 96 registers; the producer
+// group keeps 32 and the 16 consumer warps take 112, enough for their q slices
+// and accumulators without spilling.
+template <int HS>
+__host__ __device__ constexpr int block_warps() {
+  return HS == 1 ? consumer_warps<HS>() + 1 : consumer_warps<HS>() + 4;
+}
+constexpr int kSplitLaunchRegs = 96, kSplitConsumerRegs = 112, kSplitProducerRegs = 32;
+static_assert(16 * 32 * kSplitConsumerRegs + 4 * 32 * kSplitProducerRegs <= 20 * 32 * kSplitLaunchRegs,
+              "register split exceeds the launch's allotment");
+
 // Row of one split partial in the workspace: accumulator[D], m, l, and two pad
 // floats so that every row starts on a 16-byte boundary (float4 stores).
 template <int D>
@@ -603,7 +616,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
 }
 
 template <int D, int G, int HS>
-__global__ void __maxnreg__(HS == 1 ? 168 : 96) decode_split_kernel(const DecodeArgs a,
+__global__ void __maxnreg__(HS == 1 ? 168 : kSplitLaunchRegs) decode_split_kernel(const DecodeArgs a,
                                                                 const AppendArgs app) {
   constexpr int CW = consumer_warps<HS>(), GE = G / HS;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -632,10 +645,21 @@ __global__ void __maxnreg__(HS == 1 ? 168 : 96) decode_split_kernel(const Decode
     fence_mbar_init();
   }
   __syncthreads();
-  if ((threadIdx.x >> 5) == CW)
-    decode_producer<D>(a, app, ringK, ringV, meta, full, empty);
-  else
-    decode_consumer<D, GE, HS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
+  const int warp = threadIdx.x >> 5;
+  if constexpr (HS == 1) {
+    if (warp == CW)
+      decode_producer<D>(a, app, ringK, ringV, meta, full, empty);
+    else
+      decode_consumer<D, GE, HS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
+  } else {
+    if (warp >= CW) {
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSplitProducerRegs));
+      if (warp == CW) decode_producer<D>(a, app, ringK, ringV, meta, full, empty);
+    } else {
+      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSplitConsumerRegs));
+      decode_consumer<D, GE, HS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
+    }
+  }
 }
 
 // Combines the partials of every sequence that crosses a CTA boundary.
@@ -680,7 +704,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const AppendArgs& app, int ctas
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, HS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_split_kernel<D, G, HS><<<ctas, (consumer_warps<HS>() + 1) * 32, smem, stream>>>(a, app);
+  decode_split_kernel<D, G, HS><<<ctas, block_warps<HS>() * 32, smem, stream>>>(a, app);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
