@@ -53,8 +53,8 @@ N_SETS = 4
 TRAFFIC = {
     # decode B64 workload (one input set), one ncu --set full capture of the split kernel
     "decode": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu",
-               "sha256": "b88bad612cfecedb310bc514a21e8cb90a381ac7248bd2168639ae5888215b46",
-               "bytes": 569084160 + 4334848},
+               "sha256": "f8d1ff21d8ec2e4c604965a4d7b16c5ba01ab3f685d18bdbe4fb96400d080168",
+               "bytes": 569284864 + 3960320},
     # prefill workload (8 prompts, 32/8/128), one ncu --set full capture
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
                 "sha256": "e860c116ff6772463152811a00018182a6972dc0befc488142f378267eee78ad",
