@@ -513,13 +513,12 @@ __device__ void mma_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, ui
           if (more) {
             mma_qk<D>(tbase + x * kBN, dq0 + x * kQStep, dk0 + (jn & 1) * kSlotStep);
             umma_commit(&bars[B_SFULL + x]);
+          } else {
+            // O_x is final: its epilogue need not wait for the other tile's last P.
+            umma_commit(&bars[B_PVDONE + x]);
           }
           ++np[x];
         }
-      }
-      if (!more) {  // the item's O tiles are final
-        umma_commit(&bars[B_PVDONE]);
-        if (ntile == 2) umma_commit(&bars[B_PVDONE + 1]);
       }
     }
     ++nitems[0];
