@@ -57,8 +57,8 @@ TRAFFIC = {
                "bytes": 569284864 + 3960320},
     # prefill workload (8 prompts, 32/8/128), one ncu --set full capture
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
-                "sha256": "e860c116ff6772463152811a00018182a6972dc0befc488142f378267eee78ad",
-                "bytes": 122845696 + 33512704},
+                "sha256": "e6aa220923fb1e25e5dfdbacab3c0614ba9717d86a7d7d59b3208cddbafff458",
+                "bytes": 122941184 + 34071040},
 }
 
 
