@@ -692,30 +692,42 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
     scheduled by the native scheduler (prefill first, max 512 seqs / 16384
     tokens per step, 768 blocks of 256 tokens), every step running kv_store +
     prefill or decode attention on all 28 layers of a Qwen3-0.6B attention
-    shape (16/8/128).  Aggregate GB/s over the decode steps (algorithmic
+    shape (16/8/128).  Prefill steps are launched eagerly; decode steps replay
+    one 28-layer graph per batch-size bucket (LayeredDecodeGraphs), as the
+    pages' engine does.  Aggregate GB/s over the decode steps (algorithmic
     bytes) and TFLOP/s over the prefill steps (causal FLOPs), each timed by an
-    event pair around the step's 28 layers."""
+    event pair around the step's 28 layers (for decode: the metadata copies
+    into the graph's buffers and the replay)."""
     import torch
     from paged_kv_cache_125_gb300 import engine_trace as E
+    from paged_kv_cache_125_gb300.graphs import LayeredDecodeGraphs
     from paged_kv_cache_125_gb300.scheduler import NativeScheduler
     layers, hq, hkv, d, bs, nb = 28, 16, 8, 128, 256, 768
     scale = d ** -0.5
     torch.cuda.empty_cache()
     kv = torch.full((2, layers, nb, bs, hkv, d), float("nan"), dtype=torch.bfloat16, device=dev)
     sch = NativeScheduler(nb, bs, 512, 16384)
-    for i, (t, o) in enumerate(E.make_requests(256, (100, 1024), (100, 1024))):
+    reqs = E.make_requests(256, (100, 1024), (100, 1024))
+    for i, (t, o) in enumerate(reqs):
         sch.add(i, t, o)
+    max_blocks = max((len(t) + o + bs - 1) // bs for t, o in reqs)
+    graphs = LayeredDecodeGraphs([(kv[0, l_], kv[1, l_]) for l_ in range(layers)], hq, max_blocks,
+                                 max_bs=512, softmax_scale=scale, stream=stream)
     gq = torch.Generator(device=dev).manual_seed(5)
     row = hkv * d * 2
-    ws = torch.empty(kvp.attn_decode_workspace_size(512, hq, d, 4096, bs), dtype=torch.uint8, device=dev)
     recs = []
     w0 = time.perf_counter()
     while not sch.is_finished():
         ids, pre, m = sch.step()
         n = int(m.cu_seqlens_q[-1]) if pre else len(ids)
-        q = torch.randn((n, hq, d), generator=gq, device=dev).to(torch.bfloat16)
-        k = torch.randn((n, hkv, d), generator=gq, device=dev).to(torch.bfloat16)
-        v = torch.randn((n, hkv, d), generator=gq, device=dev).to(torch.bfloat16)
+        if pre:
+            q = torch.randn((n, hq, d), generator=gq, device=dev).to(torch.bfloat16)
+            k = torch.randn((n, hkv, d), generator=gq, device=dev).to(torch.bfloat16)
+            v = torch.randn((n, hkv, d), generator=gq, device=dev).to(torch.bfloat16)
+        else:  # every layer's new rows, straight into the graph's buffers
+            graphs.q[:, :n].copy_(torch.randn((layers, n, hq, d), generator=gq, device=dev))
+            graphs.k[:, :n].copy_(torch.randn((layers, n, hkv, d), generator=gq, device=dev))
+            graphs.v[:, :n].copy_(torch.randn((layers, n, hkv, d), generator=gq, device=dev))
         slots = m.slot_mapping.to(dev, non_blocking=True)
         if pre:
             cq, ck = m.cu_seqlens_q.to(dev, non_blocking=True), m.cu_seqlens_k.to(dev, non_blocking=True)
@@ -730,15 +742,14 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
                 int(((c + bs - 1) // bs).sum()) * 4 + n * 4
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        for layer in range(layers):
-            kc, vc = kv[0, layer], kv[1, layer]
-            if pre:
+        if pre:
+            for layer in range(layers):
+                kc, vc = kv[0, layer], kv[1, layer]
                 kvp.kv_store(k, v, slots, kc, vc)
                 kvp.attn_prefill_varlen(q, cq, ck, m.max_seqlen_q, m.max_seqlen_k, k=k, v=v, k_cache=kc,
                                         v_cache=vc, block_tables=bt, num_kv_heads=hkv, softmax_scale=scale)
-            else:
-                kvp.attn_decode_paged_append(q, k, v, slots, kc, vc, bt, ctx, m.max_context_len,
-                                             softmax_scale=scale, workspace=ws)
+        else:
+            graphs.run(n, slots, bt, ctx)
         b.record()
         recs.append((pre, work * layers, a, b))
         sch.postprocess([(7 * i + n) % 151936 for i in ids])
@@ -750,7 +761,7 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
     dec_work = sum(w_ for p_, w_, _, _ in recs if not p_)
     pre_work = sum(w_ for p_, w_, _, _ in recs if p_)
     n_dec = sum(1 for r in recs if not r[0])
-    del kv, ws
+    del kv, graphs
     torch.cuda.empty_cache()
     dec_gbs = dec_work / (dec_ms * 1e-3) / 1e9
     pre_tf = pre_work / (pre_ms * 1e-3) / 1e12
@@ -764,7 +775,8 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
                      "prefill": {"value": round(pre_tf, 2), "unit": "TFLOP/s", "ms": round(pre_ms, 2),
                                  "frac_of_bf16_burst": round(pre_tf / peaks["bf16_tflops"], 4)},
                      "how": "event pair around each step's 28 layers (prefill: kv_store + "
-                            "attn_prefill_varlen; decode: attn_decode_paged_append); "
+                            "attn_prefill_varlen, eager; decode: metadata copies + one 28-layer graph "
+                            "replay of attn_decode_paged_append per bucket); "
                             "inputs generated on the device before each step"}}
 
 

@@ -113,3 +113,82 @@ class DecodeGraphs:
             self.context_lens[b:pb].fill_(0)
         self.graphs[pb].replay()
         return self.out[:b]
+
+
+class LayeredDecodeGraphs:
+    """The decode step of a whole model as one graph per bucket: every layer's
+    ``attn_decode_paged_append`` in one capture, the way the pages' engine
+    captures its model forward for decode ("nano-vLLM-1", ModelRunner
+    capture_cudagraph).
+
+    ``kv_layers``: one (k_cache, v_cache) pair per layer, each
+    [num_blocks, block_size, num_kv_heads, head_dim] bf16.  The caller writes
+    each layer's new rows into ``q[l][:b]``, ``k[l][:b]``, ``v[l][:b]`` (fixed
+    buffers) and passes the step's metadata, shared by all layers, to
+    ``run``; layer l's output is ``out[l][:b]``.  The calls run one after the
+    other on one stream, so they share one workspace."""
+
+    def __init__(self, kv_layers, num_heads: int, max_blocks_per_seq: int, max_bs: int = 512,
+                 buckets: list[int] | None = None, softmax_scale: float | None = None, stream=None):
+        import torch
+        self.kv_layers = list(kv_layers)
+        nb, bs, hkv, d = self.kv_layers[0][0].shape
+        dev = self.kv_layers[0][0].device
+        n_layers = len(self.kv_layers)
+        self.num_heads, self.num_kv_heads, self.head_dim, self.block_size = num_heads, hkv, d, bs
+        self.max_bs = max_bs
+        self.buckets = buckets or default_buckets(max_bs)
+        if self.buckets[-1] > max_bs:
+            raise ValueError("a bucket exceeds max_bs")
+        self.capacity = max_blocks_per_seq * bs
+        self.scale = softmax_scale if softmax_scale is not None else d ** -0.5
+        bf16, i32 = torch.bfloat16, torch.int32
+        self.q = torch.zeros((n_layers, max_bs, num_heads, d), dtype=bf16, device=dev)
+        self.k = torch.zeros((n_layers, max_bs, hkv, d), dtype=bf16, device=dev)
+        self.v = torch.zeros((n_layers, max_bs, hkv, d), dtype=bf16, device=dev)
+        self.out = torch.zeros((n_layers, max_bs, num_heads, d), dtype=bf16, device=dev)
+        self.slots = torch.full((max_bs,), -1, dtype=i32, device=dev)
+        self.block_tables = torch.zeros((max_bs, max_blocks_per_seq), dtype=i32, device=dev)
+        self.context_lens = torch.zeros((max_bs,), dtype=i32, device=dev)
+        ws_bytes = attn_decode_workspace_size(max_bs, num_heads, d, self.capacity, bs)
+        self.workspace = torch.empty((max(ws_bytes, 1),), dtype=torch.uint8, device=dev)
+        self.stream = stream or torch.cuda.Stream(dev)
+        self.graphs = {b: self._capture(b) for b in self.buckets}
+
+    def _step(self, b: int) -> None:
+        for layer, (kc, vc) in enumerate(self.kv_layers):
+            attn_decode_paged_append(self.q[layer, :b], self.k[layer, :b], self.v[layer, :b],
+                                     self.slots[:b], kc, vc, self.block_tables[:b],
+                                     self.context_lens[:b], self.capacity, softmax_scale=self.scale,
+                                     workspace=self.workspace, out=self.out[layer, :b])
+
+    def _capture(self, b: int):
+        import torch
+        cur = torch.cuda.current_stream()
+        self.stream.wait_stream(cur)
+        with torch.cuda.stream(self.stream):
+            self._step(b)  # warm-up outside the capture
+        torch.cuda.current_stream().wait_stream(self.stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            self._step(b)
+        return g
+
+    def bucket(self, b: int) -> int:
+        return bucket_for(self.buckets, b)
+
+    def run(self, b: int, slot_mapping, block_tables, context_lens) -> int:
+        """One decode step of b sequences whose new rows the caller has written
+        into q/k/v[:, :b]; returns the bucket replayed (outputs in out[:, :b])."""
+        pb = self.bucket(b)
+        w = block_tables.shape[1]
+        if w > self.block_tables.shape[1]:
+            raise ValueError("block table wider than max_blocks_per_seq")
+        self.slots[:b].copy_(slot_mapping)
+        self.block_tables[:b, :w].copy_(block_tables)
+        self.context_lens[:b].copy_(context_lens)
+        if pb > b:  # padding rows: write nothing, read nothing
+            self.slots[b:pb].fill_(-1)
+            self.context_lens[b:pb].fill_(0)
+        self.graphs[pb].replay()
+        return pb

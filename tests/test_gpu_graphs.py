@@ -39,3 +39,43 @@ def test_bucketed_graph_decode_matches_oracle(hq, hkv, d, bs):
         # padding rows of the bucket produced zeros and wrote nothing
         pb = graphs.bucket(b)
         assert torch.all(graphs.out[b:pb].float() == 0)
+
+
+def test_layered_graph_decode_matches_oracle():
+    """Three layers in one graph per bucket (the engine's whole-model decode
+    capture): each layer's cache after the replay is bit-exact and its output
+    matches the oracle's store-then-decode on that layer."""
+    import oracle
+    from paged_kv_cache_125_gb300.graphs import LayeredDecodeGraphs
+    from parity import oracle_pool
+
+    hq, hkv, d, bs, layers = 8, 4, 128, 16, 3
+    max_bs, max_blocks = 32, 10
+    nb = max_bs * max_blocks + 4
+    caches = [(torch.empty((nb, bs, hkv, d), dtype=torch.bfloat16, device="cuda"),
+               torch.empty((nb, bs, hkv, d), dtype=torch.bfloat16, device="cuda")) for _ in range(layers)]
+    graphs = LayeredDecodeGraphs(caches, hq, max_blocks, max_bs=max_bs)
+    rng = np.random.default_rng(11)
+    for b in (1, 6, 32, 3):
+        ctx = rng.integers(1, max_blocks * bs + 1, size=b).tolist()
+        w = W.decode_workload(f"layered_b{b}", ctx, hq, hkv, d, bs, nb)
+        st, a = w.steps[0].store, w.steps[0].attn
+        qs = [(a.q.float() * (1 + 0.5 * layer)).to(torch.bfloat16) for layer in range(layers)]
+        for layer, (kc, vc) in enumerate(caches):
+            kc.fill_(float("nan"))
+            vc.fill_(float("nan"))
+            w.place_history(kc, vc)
+            graphs.q[layer, :b].copy_(qs[layer])
+            graphs.k[layer, :b].copy_(st.k)
+            graphs.v[layer, :b].copy_(st.v)
+        pb = graphs.run(b, st.slot_mapping.cuda(), a.meta.block_tables.cuda(), a.meta.context_lens.cuda())
+        torch.cuda.synchronize()
+        assert_status_ok()
+        assert pb == graphs.bucket(b)
+        kr, vr = oracle_pool(w)
+        oracle.kv_store(st.k, st.v, st.slot_mapping, kr, vr)
+        for layer, (kc, vc) in enumerate(caches):
+            assert np.array_equal(u16(kc), kr) and np.array_equal(u16(vc), vr), (b, layer)
+            ref = oracle.decode(qs[layer], kr, vr, a.meta.block_tables, a.meta.context_lens, hq, hkv,
+                                w.scale)
+            assert_attn_close(graphs.out[layer, :b], ref, f"layered decode b={b} layer {layer}")
