@@ -668,7 +668,9 @@ __global__ void __maxnreg__(HS == 1 ? 168 : kSplitLaunchRegs) decode_split_kerne
 // and the "entered" slots of the following CTAs it reaches.  One thread per
 // element of head_dim.  Launched as a programmatic dependent of the split
 // kernel: it may start while the split kernel drains and waits for the split
-// grid's completion (and memory flush) before reading anything.
+// grid's completion (and memory flush) before reading anything.  Its loads
+// take two dependent rounds: split_seq[j-1 .. j+30] (one per lane), then m, l
+// and the accumulator element of every part at once.
 template <int D>
 __global__ void __launch_bounds__(D) decode_merge_kernel(const float* __restrict__ part,
                                                          const int* __restrict__ split_seq,
@@ -676,21 +678,57 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const float* __restrict
                                                          uint16_t* __restrict__ out,
                                                          int64_t out_stride) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int j = blockIdx.x, h = blockIdx.y, e = threadIdx.x;
-  const int b = split_seq[j];
-  if (b < 0 || (j > 0 && split_seq[j - 1] == b)) return;
-  int last = j + 1;
-  while (last < ctas - 1 && split_seq[last] == b) ++last;
+  const int j = blockIdx.x, h = blockIdx.y, e = threadIdx.x, lane = e & 31;
+  const int il = j - 1 + lane;
+  const int sv = (il >= 0 && il < ctas) ? split_seq[il] : -1;
+  const int b = __shfl_sync(0xffffffffu, sv, 1);
+  if (b < 0 || __shfl_sync(0xffffffffu, sv, 0) == b) return;
+  // Bit k: the sequence also leaves CTA j + k; it ends in the first CTA that
+  // it does not leave.
+  const unsigned run = __ballot_sync(0xffffffffu, sv == b) >> 1;
+  int last = j + (__ffs(~run) - 1);
+  if (run == 0x7fffffffu)  // leaves 31 CTAs in a row: walk on
+    while (last < ctas - 1 && split_seq[last] == b) ++last;
+  if (last > ctas - 1) last = ctas - 1;
   constexpr int S = part_stride<D>();
-  float M = -INFINITY;
-  for (int i = j; i <= last; ++i)
-    M = fmaxf(M, part[(((size_t)i * 2 + (i == j ? 1 : 0)) * num_heads + h) * S + D]);
+  const int nparts = last - j + 1;
   float num = 0.f, den = 0.f;
-  for (int i = j; i <= last; ++i) {
-    const float* p = part + (((size_t)i * 2 + (i == j ? 1 : 0)) * num_heads + h) * S;
-    const float w = fast_exp2(p[D] - M);
-    num += w * p[e];
-    den += w * p[D + 1];
+  constexpr int kBatch = 8;
+  if (nparts <= kBatch) {
+    float av[kBatch], mv[kBatch], lv[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      av[k] = 0.f;
+      mv[k] = -INFINITY;
+      lv[k] = 0.f;
+      if (k < nparts) {
+        const float* p = part + (((size_t)(j + k) * 2 + (k == 0 ? 1 : 0)) * num_heads + h) * S;
+        av[k] = p[e];
+        mv[k] = p[D];
+        lv[k] = p[D + 1];
+      }
+    }
+    float M = mv[0];
+#pragma unroll
+    for (int k = 1; k < kBatch; ++k) M = fmaxf(M, mv[k]);
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      if (k < nparts) {
+        const float w = fast_exp2(mv[k] - M);
+        num += w * av[k];
+        den += w * lv[k];
+      }
+    }
+  } else {
+    float M = -INFINITY;
+    for (int i = j; i <= last; ++i)
+      M = fmaxf(M, part[(((size_t)i * 2 + (i == j ? 1 : 0)) * num_heads + h) * S + D]);
+    for (int i = j; i <= last; ++i) {
+      const float* p = part + (((size_t)i * 2 + (i == j ? 1 : 0)) * num_heads + h) * S;
+      const float w = fast_exp2(p[D] - M);
+      num += w * p[e];
+      den += w * p[D + 1];
+    }
   }
   const __nv_bfloat16 r = __float2bfloat16_rn(num / den);
   out[(int64_t)b * out_stride + (int64_t)h * D + e] = *reinterpret_cast<const uint16_t*>(&r);
