@@ -349,6 +349,15 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
                                 uint64_t* xfull, uint64_t* xfree, float* xw, float* qs_all) {
   constexpr int NCH = D / 64;  // 16-byte chunks of one row per lane
   constexpr bool kQS = q_in_smem<D, G>();
+  // Heads in pairs (2q, 2q+1): the first level of the 8-lane score reduction
+  // hands head 2q to the lanes with bit 2 of li clear and head 2q+1 to the
+  // others, so the other two levels, the running max and the exponentials run
+  // once per pair instead of once per head.  Used where the head split makes
+  // the warps issue-bound (32/8/128: 341 -> 324 us on a 128-sequence batch);
+  // at G = 2 without the split the stream is HBM-bound and the extra
+  // shuffles on the score path cost 2%.
+  constexpr bool kPair = HS == 2 && G % 2 == 0;
+  constexpr int GP = kPair ? G / 2 : 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = a.num_kv_heads;
   const int NS = kBaseWarps / Hkv;
@@ -364,6 +373,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
   float* qs = qs_all + (size_t)warp * G * D;
   float acc[G][NCH][8];
   float m[G], l[G];
+  float mo[GP], lo[GP];  // paired heads: running max and sum of this lane's head of each pair
   int b = 0;
   int s = 0;
   uint32_t ph = 0;
@@ -404,6 +414,11 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
         m[h] = -INFINITY;
         l[h] = 0.f;
       }
+#pragma unroll
+      for (int q = 0; q < GP; ++q) {
+        mo[q] = -INFINITY;
+        lo[q] = 0.f;
+      }
       if constexpr (kQS) __syncwarp();
     }
 
@@ -413,6 +428,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
     // Scores of this warp's 2 x 4 tokens for its G query heads.
     float sc[2][G];
     bool valid[2];
+    const int hb = (li >> 2) & 1;  // paired heads: this lane keeps head 2q + hb
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
       const int tl = (p * NS + sub) * 4 + tg;
@@ -421,6 +437,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
       uint4 kv[NCH];
 #pragma unroll
       for (int c = 0; c < NCH; ++c) kv[c] = kr[c * 8 + li];
+      float xs[G];  // this lane's partial dot products
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float acc0 = 0.f, acc1 = 0.f;
@@ -446,34 +463,85 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
             acc1 = r.y;
           }
         }
-        float x = acc0 + acc1;
-        x += __shfl_xor_sync(0xffffffffu, x, 1);
-        x += __shfl_xor_sync(0xffffffffu, x, 2);
-        x += __shfl_xor_sync(0xffffffffu, x, 4);
-        sc[p][h] = valid[p] ? x : -INFINITY;
+        xs[h] = acc0 + acc1;
+      }
+      if constexpr (kPair) {
+#pragma unroll
+        for (int q = 0; q < GP; ++q) {
+          float keep = hb ? xs[2 * q + 1] : xs[2 * q];
+          const float send = hb ? xs[2 * q] : xs[2 * q + 1];
+          keep += __shfl_xor_sync(0xffffffffu, send, 4);
+          keep += __shfl_xor_sync(0xffffffffu, keep, 2);
+          keep += __shfl_xor_sync(0xffffffffu, keep, 1);
+          sc[p][q] = valid[p] ? keep : -INFINITY;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          float x = xs[h];
+          x += __shfl_xor_sync(0xffffffffu, x, 1);
+          x += __shfl_xor_sync(0xffffffffu, x, 2);
+          x += __shfl_xor_sync(0xffffffffu, x, 4);
+          sc[p][h] = valid[p] ? x : -INFINITY;
+        }
       }
     }
 
-    // Online softmax: one (warp-uniform) max update per stage.
+    // Online softmax: one max update per stage (warp-uniform per head).
     float pr[2][G];
+    if constexpr (kPair) {
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float mx = fmaxf(sc[0][h], sc[1][h]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      if (mx > m[h]) {
-        const float alpha = fast_exp2(m[h] - mx);  // exp2(-inf) = 0 on the first stage
-        m[h] = mx;
-        l[h] *= alpha;
+      for (int q = 0; q < GP; ++q) {
+        float mx = fmaxf(sc[0][q], sc[1][q]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        float alpha = 1.f;
+        if (mx > mo[q]) {
+          alpha = fast_exp2(mo[q] - mx);  // exp2(-inf) = 0 on the first stage
+          mo[q] = mx;
+          lo[q] *= alpha;
+        }
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+          const float ao = __shfl_xor_sync(0xffffffffu, alpha, 4);
+          const float a0 = hb ? ao : alpha, a1 = hb ? alpha : ao;
 #pragma unroll
-        for (int c = 0; c < NCH; ++c)
+          for (int c = 0; c < NCH; ++c)
 #pragma unroll
-          for (int e = 0; e < 8; ++e) acc[h][c][e] *= alpha;
+            for (int e = 0; e < 8; ++e) {
+              acc[2 * q][c][e] *= a0;
+              acc[2 * q + 1][c][e] *= a1;
+            }
+        }
+        const float mu = mo[q] == -INFINITY ? 0.f : mo[q];
+        const float p0 = fast_exp2(sc[0][q] - mu), p1 = fast_exp2(sc[1][q] - mu);
+        lo[q] += p0 + p1;
+        const float o0 = __shfl_xor_sync(0xffffffffu, p0, 4);
+        const float o1 = __shfl_xor_sync(0xffffffffu, p1, 4);
+        pr[0][2 * q] = hb ? o0 : p0;
+        pr[0][2 * q + 1] = hb ? p0 : o0;
+        pr[1][2 * q] = hb ? o1 : p1;
+        pr[1][2 * q + 1] = hb ? p1 : o1;
       }
-      const float mu = m[h] == -INFINITY ? 0.f : m[h];
-      pr[0][h] = fast_exp2(sc[0][h] - mu);
-      pr[1][h] = fast_exp2(sc[1][h] - mu);
-      l[h] += pr[0][h] + pr[1][h];
+    } else {
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        float mx = fmaxf(sc[0][h], sc[1][h]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (mx > m[h]) {
+          const float alpha = fast_exp2(m[h] - mx);  // exp2(-inf) = 0 on the first stage
+          m[h] = mx;
+          l[h] *= alpha;
+#pragma unroll
+          for (int c = 0; c < NCH; ++c)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[h][c][e] *= alpha;
+        }
+        const float mu = m[h] == -INFINITY ? 0.f : m[h];
+        pr[0][h] = fast_exp2(sc[0][h] - mu);
+        pr[1][h] = fast_exp2(sc[1][h] - mu);
+        l[h] += pr[0][h] + pr[1][h];
+      }
     }
 
     // acc += p * v
@@ -509,6 +577,18 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
     if (!(md.flags & F_LAST)) continue;
 
     // ---- end of this CTA's segment of sequence b: reduce over the 4 token groups
+    if constexpr (kPair) {  // both heads of each pair in every lane again
+      const int hb = (li >> 2) & 1;
+#pragma unroll
+      for (int q = 0; q < GP; ++q) {
+        const float mx = __shfl_xor_sync(0xffffffffu, mo[q], 4);
+        const float lx = __shfl_xor_sync(0xffffffffu, lo[q], 4);
+        m[2 * q] = hb ? mx : mo[q];
+        m[2 * q + 1] = hb ? mo[q] : mx;
+        l[2 * q] = hb ? lx : lo[q];
+        l[2 * q + 1] = hb ? lo[q] : lx;
+      }
+    }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
