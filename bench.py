@@ -53,8 +53,8 @@ N_SETS = 4
 TRAFFIC = {
     # decode B64 workload (one input set), one ncu --set full capture of the split kernel
     "decode": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu",
-               "sha256": "f8d1ff21d8ec2e4c604965a4d7b16c5ba01ab3f685d18bdbe4fb96400d080168",
-               "bytes": 569284864 + 3960320},
+               "sha256": "4f93907f1074daa6c7b430a4cdd01872cd29ec20566fa39e4a1046f6ce825078",
+               "bytes": 569290240 + 4349696},
     # prefill workload (8 prompts, 32/8/128), one ncu --set full capture
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
                 "sha256": "e6aa220923fb1e25e5dfdbacab3c0614ba9717d86a7d7d59b3208cddbafff458",
