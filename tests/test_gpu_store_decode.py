@@ -161,14 +161,20 @@ def test_decode_out_of_range_block_is_flagged_not_read():
     assert kvp.device_status() == -6
 
 
-def test_decode_config4_full_pool_sampled():
+@pytest.mark.parametrize("fused", [False, True], ids=["two_calls", "fused_store"])
+def test_decode_config4_full_pool_sampled(fused):
     """512 sequences, Qwen3-8B heads, ~150 GB pool; outputs of a seeded sample of
-    sequences against the oracle, the stored slots bit-exact."""
+    sequences against the oracle, the stored slots bit-exact; through
+    kv_store + attn_decode_paged and through attn_decode_paged_append (the
+    call the benchmark times)."""
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
     free, _ = torch.cuda.mem_get_info()
     if free < 170e9:
         pytest.skip("needs ~160 GB of free device memory")
     w = W.config4_decode(device="cuda")
-    outs, kc, vc = run_gpu(w)
+    outs, kc, vc = run_gpu(w, fused_decode=fused)
     m = w.steps[0].attn.meta
     g = torch.Generator().manual_seed(99)
     sample = torch.randperm(512, generator=g)[:24].tolist()
@@ -192,6 +198,8 @@ def test_decode_config4_full_pool_sampled():
     ref = oracle.decode(w.steps[0].attn.q[sample].cpu(), kh, vh, W.prepare_block_tables(tables),
                         torch.tensor(ctxs, dtype=torch.int32), 32, 8, w.scale)
     assert_attn_close(outs[0][sample], ref, "config4 sample")
+    del outs, kc, vc, kh, vh
+    torch.cuda.empty_cache()
 
 
 # --------------------------------------------------------------------------- fused store + decode
