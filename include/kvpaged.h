@@ -164,7 +164,11 @@ int kv_copy_blocks(kvp_bf16 *cache, int64_t num_planes, int64_t plane_stride, in
  *   out             [total_q, num_heads, head_dim] bf16, row stride out_stride_tok
  * Supported: head_dim in {64, 128}; num_heads / num_kv_heads in {1, 2, 4, 8};
  * block_size 16 * 2^k (16..4096).  q_len = 0 for a sequence is allowed (no
- * rows).  No workspace.
+ * rows).  No workspace: the CTAs share their work through a counter in one
+ * of 64 library-owned slots per device (one slot per call, in turn), so at
+ * most 64 attn_prefill_varlen calls may be in flight on a device at the same
+ * time (calls on one stream follow each other and are always fine; CUDA-graph
+ * replays of a captured call are fine too).
  */
 int attn_prefill_varlen(const kvp_bf16 *q, int64_t q_stride_tok, int64_t total_q,
                         const kvp_bf16 *k, const kvp_bf16 *v, int64_t kv_stride_tok,

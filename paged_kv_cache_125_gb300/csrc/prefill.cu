@@ -18,7 +18,10 @@
 // halves the K/V bytes moved per FLOP compared with one tile.
 //
 // Persistent CTAs (one per SM), 12 warps:
-//   warp 8  TMA producer: the Q pair (one slot), K tiles (2 slots), V tiles
+//   warp 8  picks the CTA's items (next position of the cost-sorted order
+//           from a global counter, heaviest first) and passes each to the
+//           other roles through a 2-slot ring in shared memory; and is the
+//           TMA producer: the Q pair (one slot), K tiles (2 slots), V tiles
 //           (2 slots).  In paged mode a kv tile is loaded as block-sized
 //           sub-boxes addressed through the block table (gather folded into
 //           the loads); sub-boxes past the sequence's last key are skipped.
@@ -43,6 +46,7 @@
 // columns, which S_X(j+1) overwrites, have been read).
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "kvp_device.cuh"
@@ -82,8 +86,11 @@ struct PrefillArgs {
   int tok_per_tile;  // 128 / G
   int sub_rows;      // rows per TMA box of a kv tile (paged: min(bs, 128))
   int max_pairs;     // ceil(max_seqlen_q / (2 * tok_per_tile))
-  int use_list;      // 1: items dealt by the cost-sorted schedule; 0: round-robin
+  int dynamic;       // 1: items taken in cost order from a global counter; 0: round-robin
   int cu_in_smem;    // 1: cu_seqlens_q/k are copied into shared memory at kernel start
+  unsigned long long* qslot;  // dynamic: (epoch << 32) | next position, one slot per launch
+  unsigned int* qdone;        // dynamic: CTAs finished, for the slot's reset
+  uint32_t epoch;             // dynamic: this launch's tag in the slot (>= 1)
   float scale_log2;
   uint16_t* out;
   int64_t out_stride;
@@ -98,19 +105,22 @@ struct Item {
 };
 
 constexpr int kCostBins = 256;
-constexpr int kMaxListItems = 128;
 constexpr int kCuCap = 520;  // cu_seqlens entries cached in shared memory (num_seqs + 1)
-constexpr int kMaxPairs = 8192;  // (pair rank, sequence) entries the cost-sorted deal handles
+constexpr int kMaxPairs = 4096;  // (pair rank, sequence) entries the cost-sorted order handles
+constexpr int kQueueSlots = 64;  // counter slots: prefill calls that may be in flight at once
+// Arrivals that free a slot of the item ring: the MMA thread, the 8 softmax
+// warps and the V fix-up warp.
+constexpr int kItemReaders = 10;
 
-// Per-CTA schedule state in shared memory (written before the roles start).
+// Per-CTA schedule state in shared memory.
 struct Sched {
   uint32_t bins[kCostBins];  // histogram, then next free position per cost
-  int count;
+  int count;                 // item positions of the cost-sorted order
   int pad[3];
-  int items[kMaxListItems];   // item indices dealt to this CTA
-  Item list[kMaxListItems];   // the same items, decoded
-  int cu[2][kCuCap];          // cu_seqlens_q, cu_seqlens_k
-  uint8_t cost[kMaxPairs];    // cost bin of each (rank, sequence) pair, 0 = no work
+  Item ring[2];              // items passed from the producer to the other roles
+  int cu[2][kCuCap];         // cu_seqlens_q, cu_seqlens_k
+  uint8_t cost[kMaxPairs];   // cost bin of each (rank, sequence) pair, 0 = no work
+  uint16_t order[kMaxPairs]; // pair index at each pair position of the cost-sorted order
 };
 constexpr uint32_t kSchedBytes = (sizeof(Sched) + 15) & ~15u;
 
@@ -124,7 +134,7 @@ struct Layout {
   static constexpr uint32_t kK = kQ + 2 * kQBytes;   // 2 slots
   static constexpr uint32_t kV = kK + 2 * kKVBytes;  // 2 slots
   static constexpr uint32_t kBar = kV + 2 * kKVBytes;
-  static constexpr uint32_t kNumBars = 21;
+  static constexpr uint32_t kNumBars = 25;
   static constexpr uint32_t kSched = kBar + kNumBars * 8 + 16;
   static constexpr uint32_t kTotal = kSched + kSchedBytes;
   // The dynamic shared memory base is 1 KiB aligned on this architecture (the
@@ -146,7 +156,9 @@ enum : int {
   B_PVDONE = 14, // [2]
   B_OFREE = 16,  // [2]
   B_VREADY = 18, // [2]: V tile loaded and its rows past the last key zeroed
-  B_DRAIN = 20,
+  B_IFULL = 20,  // [2]: item ring slot written by the producer
+  B_IEMPTY = 22, // [2]: item ring slot read by every other role
+  B_DRAIN = 24,
 };
 
 // cu_seqlens as the roles read them: from shared memory when cached there.
@@ -193,12 +205,13 @@ __device__ __forceinline__ int total_items(const PrefillArgs& a) {
   return a.max_pairs * a.num_seqs * a.num_kv_heads;
 }
 
-// Per-CTA work list.  An item's cost (kv tiles x query tiles) depends only on
-// its sequence and pair rank, not on the kv head, so the schedule is built
-// over (rank, sequence) pairs: every CTA computes the same cost histogram,
-// ranks the pairs by cost (ties in index order), and keeps the items that a
-// snake deal of the sorted list (0..P-1, P-1..0, ...) gives it.  Greedy on the
-// sorted order keeps the heaviest SM close to the average.
+// Work order.  An item's cost (kv tiles x query tiles) depends only on its
+// sequence and pair rank, not on the kv head, so the order is built over
+// (rank, sequence) pairs: every CTA computes the same cost histogram and ranks
+// the pairs by cost (ties in index order).  The CTAs then take items from that
+// order, heaviest first, through one global counter per launch: a CTA takes
+// the next item whenever it is ready (greedy list scheduling), which keeps
+// the SMs' finish times together whatever the length mix.
 __device__ __forceinline__ bool pair_cost(const PrefillArgs& a, const Cu& cu, int idx, int& v) {
   const int r = idx / a.num_seqs, b = idx - r * a.num_seqs;
   const int q_len = cu.q[b + 1] - cu.q[b];
@@ -227,10 +240,10 @@ __device__ void schedule_costs(const PrefillArgs& a, Sched* sc) {
       sc->cu[0][i] = a.cu_q[i];
       sc->cu[1][i] = a.cu_k[i];
     }
-  if (a.use_list)
+  if (a.dynamic)
     for (int i = tid; i < kCostBins; i += nt) sc->bins[i] = 0;
   __syncthreads();
-  if (!a.use_list) return;
+  if (!a.dynamic) return;
   const Cu cu = cu_view(a, sc);
   const int npi = a.max_pairs * a.num_seqs;
   for (int idx = tid; idx < npi; idx += nt) {
@@ -242,15 +255,12 @@ __device__ void schedule_costs(const PrefillArgs& a, Sched* sc) {
   __syncthreads();
 }
 
-// Second part, one warp: positions in the cost-sorted order and this CTA's
-// share of the snake deal, then the dealt items decoded.  Position p goes to
-// CTA p mod 2P when that is < P, else to 2P - 1 - (p mod 2P); so this CTA's
-// k-th item sits at position (k / 2) * 2P + (k even ? bx : 2P - 1 - bx), and
-// the list comes out in position order (heaviest first) without sorting.
-__device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
+// Second part, one warp (the producer's): the cost-sorted order.  Pairs are
+// ranked by cost, descending, ties in index order; a pair's Hkv items take
+// consecutive positions, and order[] maps a pair position back to the pair.
+__device__ void build_order(const PrefillArgs& a, Sched* sc) {
   const int lane = threadIdx.x & 31;
-  const Cu cu = cu_view(a, sc);
-  const uint32_t H = a.num_kv_heads, P2 = 2 * gridDim.x, bx = blockIdx.x;
+  const uint32_t H = a.num_kv_heads;
   const int npi = a.max_pairs * a.num_seqs;
   // Exclusive prefix in descending cost: lane 0 owns the 8 highest bins.
   const int base = (31 - lane) * 8;
@@ -273,7 +283,6 @@ __device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
     run += c;
   }
   __syncwarp();
-  // Positions in (rank, sequence) order; equal costs keep index order.
   for (int b0 = 0; b0 < npi; b0 += 32) {
     const int idx = b0 + lane;
     const int v = idx < npi ? sc->cost[idx] : 0;
@@ -284,41 +293,52 @@ __device__ void build_schedule(const PrefillArgs& a, Sched* sc) {
     if (ok) pos0 = sc->bins[v] + (uint32_t)__popc(lower) * H;
     __syncwarp();
     if (ok && lower == 0) sc->bins[v] += (uint32_t)__popc(same) * H;
-    if (ok) {
-      const uint32_t per = pos0 / P2;
-      for (uint32_t q = per;; ++q) {
-        const uint32_t c0 = q * P2 + bx, c1 = q * P2 + (P2 - 1 - bx);
-        if (c0 >= pos0 + H) break;
-        if (c0 >= pos0 && 2 * q < (uint32_t)kMaxListItems)
-          sc->items[2 * q] = idx * (int)H + (int)(c0 - pos0);
-        if (c1 >= pos0 && c1 < pos0 + H && 2 * q + 1 < (uint32_t)kMaxListItems)
-          sc->items[2 * q + 1] = idx * (int)H + (int)(c1 - pos0);
-      }
-    }
+    if (ok) sc->order[pos0 / H] = (uint16_t)idx;
     __syncwarp();
   }
-  const uint32_t rem = total % P2;
-  const int n = min((int)(2 * (total / P2) + (rem > bx) + (rem > P2 - 1 - bx)), kMaxListItems);
-  if (lane == 0) sc->count = n;
-  for (int i = lane; i < n; i += 32) decode_item(a, cu, sc->items[i], sc->list[i]);
+  if (lane == 0) sc->count = (int)total;
   __syncwarp();
 }
 
-// Next item of this CTA: from the work list, or round-robin over all items.
-// `cursor` starts at 0 and is advanced past the returned item.
-__device__ __forceinline__ bool next_item(const PrefillArgs& a, const Sched* sc, int& cursor,
-                                          Item& it) {
-  if (a.use_list) {
-    if (cursor >= min(sc->count, kMaxListItems)) return false;
-    it = sc->list[cursor++];
-    return true;
+// Next position of the cost-sorted order for this launch (one thread).  The
+// slot holds (epoch << 32) | next position.  A slot still tagged with another
+// epoch (zero after the previous launch on it reset it, or an older launch
+// that stopped early) is moved to this launch's epoch at position 0: a CAS
+// against the value last seen, repeated against the value it returns until
+// the slot carries this epoch (whichever CTA's CAS lands first does it; an
+// increment that lands after it is already a position of this launch).
+__device__ __forceinline__ int queue_fetch(const PrefillArgs& a) {
+  unsigned long long v = atomicAdd(a.qslot, 1ull);
+  if ((uint32_t)(v >> 32) == a.epoch) return (int)(v & 0xffffffffull);
+  const unsigned long long fresh = (unsigned long long)a.epoch << 32;
+  unsigned long long cur = v + 1ull;
+  for (int tries = 0; (uint32_t)(cur >> 32) != a.epoch; ++tries) {
+    if (tries > 4096) {
+      record_error(a.status, KVP_ERR_DEVICE_TIMEOUT);
+      return 0x7fffffff;
+    }
+    const unsigned long long prev = atomicCAS(a.qslot, cur, fresh);
+    cur = prev == cur ? fresh : prev;
   }
-  const Cu cu = cu_view(a, sc);
-  for (int L = blockIdx.x + cursor * (int)gridDim.x; L < total_items(a); L += gridDim.x) {
-    ++cursor;
-    if (decode_item(a, cu, L, it)) return true;
+  v = atomicAdd(a.qslot, 1ull);
+  if ((uint32_t)(v >> 32) != a.epoch) {  // another launch on this slot: not allowed
+    record_error(a.status, KVP_ERR_DEVICE_DATA);
+    return 0x7fffffff;
   }
-  return false;
+  return (int)(v & 0xffffffffull);
+}
+
+// Item k of this CTA, from the producer's ring; false at the end marker (or
+// if the wait expired).  The copy is taken before the slot is freed: one
+// arrive per reading warp after __syncwarp, or by the MMA thread itself.
+__device__ __forceinline__ bool ring_item(const Sched* sc, uint64_t* bars, int k, Item& it,
+                                          bool warp_wide, int* status) {
+  const int rs = k & 1;
+  if (!mbar_wait(&bars[B_IFULL + rs], (k >> 1) & 1, status)) return false;
+  it = sc->ring[rs];
+  if (warp_wide) __syncwarp();
+  if (!warp_wide || (threadIdx.x & 31) == 0) mbar_arrive(&bars[B_IEMPTY + rs]);
+  return it.b >= 0;
 }
 
 // Transpose of a 4 x 4 matrix of 16-byte chunks held by the 4 lanes of a
@@ -357,8 +377,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 template <int D>
 __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                              const CUtensorMap* tmV, uint8_t* smem, uint64_t* bars,
-                              const Sched* sc) {
+                              const CUtensorMap* tmV, uint8_t* smem, uint64_t* bars, Sched* sc) {
   using Lay = Layout<D>;
   const int lane = threadIdx.x & 31;
   if (lane == 0) {
@@ -366,10 +385,49 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
     prefetch_tensormap(tmK);
     prefetch_tensormap(tmV);
   }
+  if (a.dynamic) build_order(a, sc);
+  const Cu cu = cu_view(a, sc);
+  // The producer picks this CTA's items and hands each to the other roles
+  // through the 2-slot item ring.  Dynamic mode: the next position of the
+  // cost-sorted order from the launch's counter, so the heaviest items go
+  // first and a CTA takes another one whenever it is ready; the next
+  // position is fetched while the current item loads.  Otherwise round-robin
+  // over all item indices.
+  int next_pos = 0, rr = 0;
+  if (a.dynamic && lane == 0) next_pos = queue_fetch(a);
   int item_idx = 0;
   uint32_t jt = 0;
   Item it;
-  for (int cur = 0; next_item(a, sc, cur, it); ++item_idx) {
+  for (;; ++item_idx) {
+    bool have = false;
+    if (a.dynamic) {
+      int pos = __shfl_sync(0xffffffffu, next_pos, 0);
+      while (pos < sc->count) {
+        const int H = a.num_kv_heads;
+        have = decode_item(a, cu, (int)sc->order[pos / H] * H + pos % H, it);
+        if (lane == 0) next_pos = queue_fetch(a);
+        if (have) break;
+        pos = __shfl_sync(0xffffffffu, next_pos, 0);
+      }
+    } else {
+      for (int L = blockIdx.x + rr * (int)gridDim.x; L < total_items(a); L += gridDim.x) {
+        ++rr;
+        if (decode_item(a, cu, L, it)) {
+          have = true;
+          break;
+        }
+      }
+    }
+    const int rs = item_idx & 1;
+    if (!mbar_wait(&bars[B_IEMPTY + rs], ((item_idx >> 1) & 1) ^ 1u, a.status)) return;
+    if (lane == 0) {
+      if (have)
+        sc->ring[rs] = it;
+      else
+        sc->ring[rs].b = -1;  // end marker
+      mbar_arrive(&bars[B_IFULL + rs]);
+    }
+    if (!have) break;
     // Q pair: both tiles in one slot (tile B past the sequence is harmless
     // data: its rows are never stored).
     if (!mbar_wait(&bars[B_QEMPTY], (item_idx & 1) ^ 1u, a.status)) return;
@@ -483,7 +541,7 @@ __device__ void mma_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, ui
   int item_idx = 0;
   uint32_t jt = 0;
   Item it;
-  for (int cur = 0; next_item(a, sc, cur, it); ++item_idx) {
+  for (; ring_item(sc, bars, item_idx, it, false, a.status); ++item_idx) {
     const int ntile = it.rows_b > 0 ? 2 : 1;
     if (!mbar_wait(&bars[B_QFULL], item_idx & 1, a.status)) goto drain;
     if (!mbar_wait(&bars[B_KFULL + (jt & 1)], (jt >> 1) & 1, a.status)) goto drain;
@@ -541,7 +599,7 @@ __device__ void vfix_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, c
   const int lane = threadIdx.x & 31;
   uint32_t jt = 0;
   Item it;
-  for (int cur = 0; next_item(a, sc, cur, it);) {
+  for (int k = 0; ring_item(sc, bars, k, it, true, a.status); ++k) {
     for (int j = 0; j < it.n_tiles; ++j, ++jt) {
       const int st = jt & 1;
       if (!mbar_wait(&bars[B_VFULL + st], (jt >> 1) & 1, a.status)) return;
@@ -583,7 +641,7 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
   // earlier MMA that read those slots.
   const bool releaser = (warp & 3) == 0 && lane == 0;
   Item it;
-  for (int cur = 0; next_item(a, sc, cur, it); jt0 += it.n_tiles) {
+  for (int k = 0; ring_item(sc, bars, k, it, true, a.status); ++k, jt0 += it.n_tiles) {
     const bool has_b = it.rows_b > 0;
     const int rows = x == 0 ? it.rows_a : it.rows_b;
     if (x == 1 && !has_b) continue;
@@ -745,7 +803,6 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
   Sched* sc = reinterpret_cast<Sched*>(smem + Lay::kSched);
   const int warp = threadIdx.x >> 5;
   schedule_costs(a, sc);
-  if (warp == kProducerWarp && a.use_list) build_schedule(a, sc);
 
   if (threadIdx.x == 0) {
     mbar_init(&bars[B_QFULL], 1);
@@ -760,6 +817,8 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
       mbar_init(&bars[B_PVDONE + i], 1);
       mbar_init(&bars[B_OFREE + i], 4);
       mbar_init(&bars[B_VREADY + i], 1);
+      mbar_init(&bars[B_IFULL + i], 1);
+      mbar_init(&bars[B_IEMPTY + i], kItemReaders);
     }
     mbar_init(&bars[B_DRAIN], 1);
     fence_mbar_init();
@@ -790,9 +849,53 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tbase, 512);
+  if (a.dynamic && threadIdx.x == 0) {
+    // Every fetch of this CTA is done.  The last CTA to get here returns the
+    // counter slot to zero, so the same launch parameters (a CUDA graph
+    // replay) start from position 0 again.
+    __threadfence();
+    if (atomicAdd(a.qdone, 1u) == gridDim.x - 1) {
+      atomicExch(a.qslot, 0ull);
+      atomicExch(a.qdone, 0u);
+    }
+  }
 }
 
+// Counter slots of the dynamic schedule: one per prefill launch in flight
+// (launch n uses slot n % kQueueSlots with epoch n / kQueueSlots + 1).
+__device__ unsigned long long g_queue_slot[kQueueSlots];
+__device__ unsigned int g_queue_done[kQueueSlots];
+
 // ------------------------------------------------------------------ host side
+
+// Device addresses of the counter slots (looked up once per device) and the
+// launch sequence number per device.
+constexpr int kMaxQueueDevices = 64;
+unsigned long long* g_qslot_ptr[kMaxQueueDevices];
+unsigned int* g_qdone_ptr[kMaxQueueDevices];
+std::atomic<unsigned long long> g_qseq[kMaxQueueDevices];
+std::mutex g_queue_mutex;
+
+bool queue_slots(unsigned long long** slots, unsigned int** dones, unsigned long long* seq) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxQueueDevices) return false;
+  {
+    std::lock_guard<std::mutex> lock(g_queue_mutex);
+    if (!g_qslot_ptr[dev]) {
+      void* ps = nullptr;
+      void* pd = nullptr;
+      if (cudaGetSymbolAddress(&ps, g_queue_slot) != cudaSuccess ||
+          cudaGetSymbolAddress(&pd, g_queue_done) != cudaSuccess)
+        return false;
+      g_qdone_ptr[dev] = static_cast<unsigned int*>(pd);
+      g_qslot_ptr[dev] = static_cast<unsigned long long*>(ps);
+    }
+  }
+  *slots = g_qslot_ptr[dev];
+  *dones = g_qdone_ptr[dev];
+  *seq = g_qseq[dev].fetch_add(1);
+  return true;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -903,10 +1006,22 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
     return KVP_ERR_UNSUPPORTED;
   }
   const int grid = (int)(items < num_sms ? items : num_sms);
-  a.use_list = items <= (long long)kMaxListItems * grid &&
-                       (long long)a.max_pairs * num_seqs <= kMaxPairs
-                   ? 1
-                   : 0;
+  a.dynamic = (long long)a.max_pairs * num_seqs <= kMaxPairs ? 1 : 0;
+  a.qslot = nullptr;
+  a.qdone = nullptr;
+  a.epoch = 0;
+  if (a.dynamic) {
+    unsigned long long* slots;
+    unsigned int* dones;
+    unsigned long long seq;
+    if (!queue_slots(&slots, &dones, &seq)) {
+      *why = "counter slots of the dynamic schedule unavailable";
+      return KVP_ERR_CUDA;
+    }
+    a.qslot = slots + seq % kQueueSlots;
+    a.qdone = dones + seq % kQueueSlots;
+    a.epoch = (uint32_t)(seq / kQueueSlots) + 1u;
+  }
   a.cu_in_smem = num_seqs + 1 <= kCuCap ? 1 : 0;
   cudaError_t e = head_dim == 128 ? launch_t<128>(mq, mk, mv, a, grid, stream)
                                   : launch_t<64>(mq, mk, mv, a, grid, stream);

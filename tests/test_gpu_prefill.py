@@ -111,3 +111,61 @@ def test_prefill_scores_growing_across_tiles(cached_blocks, hq, hkv):
     st.k.copy_(keys(list(range(c, L))))
     a.q.copy_((0.25 + 0.05 * torch.randn(a.q.shape, generator=g)).to(torch.bfloat16))
     _check(w)
+
+
+def _prefill_inputs(w):
+    import types
+    from parity import gpu_pool
+    kc, vc = gpu_pool(w)
+    for st in w.setup:
+        kvp.kv_store(st.k.cuda(), st.v.cuda(), st.slot_mapping.cuda(), kc, vc)
+    s, a = w.steps[0].store, w.steps[0].attn
+    kvp.kv_store(s.k.cuda(), s.v.cuda(), s.slot_mapping.cuda(), kc, vc)
+    m = a.meta
+    return types.SimpleNamespace(
+        q=a.q.cuda(), k=a.k.cuda(), v=a.v.cuda(), kc=kc, vc=vc, cq=m.cu_seqlens_q.cuda(),
+        ck=m.cu_seqlens_k.cuda(), mq=m.max_seqlen_q, mk=m.max_seqlen_k,
+        bt=None if m.block_tables is None else m.block_tables.cuda(),
+        out=torch.empty_like(a.q.cuda()))
+
+
+def _prefill_call(x, w):
+    kvp.attn_prefill_varlen(x.q, x.cq, x.ck, x.mq, x.mk, k=x.k, v=x.v, k_cache=x.kc, v_cache=x.vc,
+                            block_tables=x.bt, num_kv_heads=w.num_kv_heads, softmax_scale=w.scale,
+                            out=x.out)
+
+
+def test_prefill_graph_replays_repeat_the_schedule():
+    """The work counter of a launch is reset by its last CTA, so a captured
+    prefill call gives the full result on every replay."""
+    w = W.prefill_workload("graph_replay", [700, 1500, 90, 2048], [1, 0, 0, 2], 32, 8, 128, 256, 64)
+    x = _prefill_inputs(w)
+    ref, _, _ = run_oracle(w)
+    _prefill_call(x, w)  # first use outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        _prefill_call(x, w)
+    for rep in range(3):
+        x.out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert_status_ok()
+        assert_attn_close(x.out, ref[0], f"graph replay {rep}")
+
+
+def test_prefill_many_launches_reuse_counter_slots():
+    """More launches than counter slots: every slot is used again with a new
+    epoch; the last launch still covers every item."""
+    w = W.prefill_workload("many_launches", [300, 33, 1100], [0, 0, 1], 16, 8, 128, 256, 16)
+    x = _prefill_inputs(w)
+    ref, _, _ = run_oracle(w)
+    for i in range(140):
+        if i == 139:
+            x.out.fill_(float("nan"))
+        _prefill_call(x, w)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    assert_attn_close(x.out, ref[0], "launch 140")
