@@ -57,8 +57,8 @@ TRAFFIC = {
                "bytes": 569290240 + 4349696},
     # prefill workload (8 prompts, 32/8/128), one ncu --set full capture
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
-                "sha256": "e6aa220923fb1e25e5dfdbacab3c0614ba9717d86a7d7d59b3208cddbafff458",
-                "bytes": 122941184 + 34071040},
+                "sha256": "f69c4737de03eae7db2c5ef877ef514274986dce2b90bcfc9ace51bd1dfa44c9",
+                "bytes": 123229440 + 34801408},
 }
 
 
