@@ -307,6 +307,8 @@ __device__ void build_order(const PrefillArgs& a, Sched* sc) {
 // against the value last seen, repeated against the value it returns until
 // the slot carries this epoch (whichever CTA's CAS lands first does it; an
 // increment that lands after it is already a position of this launch).
+// Positions stay below 2^15 (at most kMaxPairs x 8 items); 0x3fffffff means
+// none (an error was recorded).
 __device__ __forceinline__ int queue_fetch(const PrefillArgs& a) {
   unsigned long long v = atomicAdd(a.qslot, 1ull);
   if ((uint32_t)(v >> 32) == a.epoch) return (int)(v & 0xffffffffull);
@@ -315,7 +317,7 @@ __device__ __forceinline__ int queue_fetch(const PrefillArgs& a) {
   for (int tries = 0; (uint32_t)(cur >> 32) != a.epoch; ++tries) {
     if (tries > 4096) {
       record_error(a.status, KVP_ERR_DEVICE_TIMEOUT);
-      return 0x7fffffff;
+      return 0x3fffffff;
     }
     const unsigned long long prev = atomicCAS(a.qslot, cur, fresh);
     cur = prev == cur ? fresh : prev;
@@ -323,7 +325,7 @@ __device__ __forceinline__ int queue_fetch(const PrefillArgs& a) {
   v = atomicAdd(a.qslot, 1ull);
   if ((uint32_t)(v >> 32) != a.epoch) {  // another launch on this slot: not allowed
     record_error(a.status, KVP_ERR_DEVICE_DATA);
-    return 0x7fffffff;
+    return 0x3fffffff;
   }
   return (int)(v & 0xffffffffull);
 }
@@ -393,8 +395,9 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
   // first and a CTA takes another one whenever it is ready; the next
   // position is fetched while the current item loads.  Otherwise round-robin
   // over all item indices.
-  int next_pos = 0, rr = 0;
-  if (a.dynamic && lane == 0) next_pos = queue_fetch(a);
+  // The first item of CTA bx is position bx, without a fetch; the counter
+  // hands out positions from gridDim.x on.
+  int next_pos = blockIdx.x, rr = 0;
   int item_idx = 0;
   uint32_t jt = 0;
   Item it;
@@ -405,7 +408,7 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
       while (pos < sc->count) {
         const int H = a.num_kv_heads;
         have = decode_item(a, cu, (int)sc->order[pos / H] * H + pos % H, it);
-        if (lane == 0) next_pos = queue_fetch(a);
+        if (lane == 0) next_pos = (int)gridDim.x + queue_fetch(a);
         if (have) break;
         pos = __shfl_sync(0xffffffffu, next_pos, 0);
       }
