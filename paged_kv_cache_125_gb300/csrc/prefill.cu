@@ -778,8 +778,12 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
       for (int k = 0; k < 4; ++k)
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          w[k][i] = pack_bf16x2(__uint_as_float(ov[c][8 * k + 2 * i]) * inv,
-                                __uint_as_float(ov[c][8 * k + 2 * i + 1]) * inv);
+          {
+            const float2 o = __fmul2_rn(make_float2(__uint_as_float(ov[c][8 * k + 2 * i]),
+                                                    __uint_as_float(ov[c][8 * k + 2 * i + 1])),
+                                        make_float2(inv, inv));
+            w[k][i] = pack_bf16x2(o.x, o.y);
+          }
       quad_transpose16(w, lane);
 #pragma unroll
       for (int k = 0; k < 4; ++k)
