@@ -169,3 +169,24 @@ def test_prefill_many_launches_reuse_counter_slots():
     torch.cuda.synchronize()
     assert_status_ok()
     assert_attn_close(x.out, ref[0], "launch 140")
+
+
+def test_prefill_concurrent_streams_use_separate_counters():
+    """Two prefill calls in flight at once on two streams take different
+    counter slots; both results are complete."""
+    w1 = W.prefill_workload("streams_a", [900, 400, 1500], [1, 0, 2], 32, 8, 128, 256, 32)
+    w2 = W.prefill_workload("streams_b", [2048, 77], [0, 0], 16, 8, 128, 256, 16)
+    x1, x2 = _prefill_inputs(w1), _prefill_inputs(w2)
+    r1, _, _ = run_oracle(w1)
+    r2, _, _ = run_oracle(w2)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    for rep in range(20):
+        with torch.cuda.stream(s1):
+            _prefill_call(x1, w1)
+        with torch.cuda.stream(s2):
+            _prefill_call(x2, w2)
+    torch.cuda.synchronize()
+    assert_status_ok()
+    assert_attn_close(x1.out, r1[0], "stream 1")
+    assert_attn_close(x2.out, r2[0], "stream 2")
