@@ -406,7 +406,8 @@ def oracle_decode_rate(w, min_seconds=8.0):
 def run_reference(args, rank, world):
     """The oracle as it stands, timed on the host cores, on the same workload and
     metric: each step is the full decode step (store + decode of all 64
-    sequences); at most --steps steps and about 60 s of timed work."""
+    sequences); --warmup untimed steps (at least 3, then up to ~20 s), then at
+    most --steps steps and about 60 s of timed work."""
     if rank != 0:
         return
     sys.path.insert(0, os.path.join(ROOT, "tests"))
@@ -422,8 +423,10 @@ def run_reference(args, rank, world):
         oracle.kv_store(st.k, st.v, st.slot_mapping, kc, vc)
         oracle.decode(a.q, kc, vc, m.block_tables, m.context_lens, w.num_heads, w.num_kv_heads, w.scale)
 
-    for _ in range(min(args.warmup, 1)):
+    warm, tw = 0, time.perf_counter()
+    while warm < args.warmup and (warm < 3 or time.perf_counter() - tw < 20.0):
         step()
+        warm += 1
     done, t0 = 0, time.perf_counter()
     while done < args.steps and (done == 0 or time.perf_counter() - t0 < 60.0):
         step()
@@ -433,7 +436,7 @@ def run_reference(args, rank, world):
     value = (store + dec) * done / el / 1e9
     cores = oracle.num_threads()
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
-            "n_gpus": args.gpus, "steps": done, "warmup": min(args.warmup, 1),
+            "n_gpus": args.gpus, "steps": done, "warmup": warm,
             "ms_per_step": round(1000 * el / done, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.description, "parallelism": f"{cores} host threads"},
