@@ -53,7 +53,7 @@ N_SETS = 4
 TRAFFIC = {
     # decode B64 workload (one input set), one ncu --set full capture of the split kernel
     "decode": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu",
-               "sha256": "4f93907f1074daa6c7b430a4cdd01872cd29ec20566fa39e4a1046f6ce825078",
+               "sha256": "433d40b20eb179859e88382bab3348e25d4f55996ec0a81e4422bd574c42a5b1",
                "bytes": 569290240 + 4349696},
     # prefill workload (8 prompts, 32/8/128), one ncu --set full capture
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",

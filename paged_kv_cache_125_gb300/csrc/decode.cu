@@ -26,11 +26,16 @@
 //   chunks at head_dim 128) of one token; 4 tokens per pass.  q . k is an
 //   fp32 dot product over the lane's slice reduced over 8 lanes by shuffles,
 //   with q pre-scaled by softmax_scale * log2(e) so the softmax uses exp2.
-//   The running max is warp-uniform and updated once per stage.
+//   The running max is warp-uniform and updated once per stage.  Where
+//   G * head_dim >= 512 the query heads of a kv head are split over two
+//   warps (16 consumer warps, see head_split), the producer gets a warpgroup
+//   of its own that hands registers to the consumers (setmaxnreg), and the
+//   score reduction runs on pairs of heads.
 // * Optional store of the step's new rows (attn_decode_paged_append): the
 //   kv_store of one new token per sequence is folded into the same launch.
-//   CTA i writes the rows of sequences i, i + P, ... into the cache slots
-//   slot_mapping[b]; the stage that ends at a sequence's last context token
+//   After the producer has issued every stage, its warp writes the rows of
+//   sequences i, i + P, ... (CTA i) into the cache slots slot_mapping[b];
+//   the stage that ends at a sequence's last context token
 //   takes that token's K and V row straight from the new rows (one more bulk
 //   copy) instead of from the cache, so no CTA reads a slot written in the
 //   same launch.
