@@ -610,10 +610,14 @@ def measure_mixed(args, kvp, W, dev, stream, world, peaks):
 
 def measure_bucketed(args, kvp, W, dev, stream, world, peaks):
     """The engine's graph-replayed decode with batch-size buckets: a step of
-    50 sequences (16/8/128, bs 256, ctx U[512, 4096], 2048-block pool) copies
-    its inputs into the fixed buffers and replays the bucket-64 graph (14
-    padding rows: slot -1, context 0).  Value = algorithmic bytes of the 50
-    real sequences / step time."""
+    50 sequences (16/8/128, bs 256, ctx U[512, 4096], 2048-block pool) loads
+    its metadata (slot_mapping, context_lens, block tables, packed for the
+    bucket with its 14 padding rows: slot -1, context 0) in one copy from
+    pinned host memory and replays the bucket-64 graph.  q, k and v sit in the
+    graph's fixed buffers, where an engine's projections write them.  Value =
+    algorithmic bytes of the 50 real sequences / step time.  A second loop
+    times ``run`` with every input (q, k, v and metadata) copied from device
+    tensors into the graph's buffers, as separate copies."""
     import torch
     from paged_kv_cache_125_gb300.graphs import DecodeGraphs
     g = torch.Generator().manual_seed(W.SEED_LENGTHS)
@@ -623,33 +627,53 @@ def measure_bucketed(args, kvp, W, dev, stream, world, peaks):
     w.place_history(kc, vc)
     graphs = DecodeGraphs(kc, vc, 16, 16, max_bs=64, stream=stream)
     st, a = w.steps[0].store, w.steps[0].attn
+    b = len(ctx)
     ins = [a.q.to(dev), st.k.to(dev), st.v.to(dev), st.slot_mapping.to(dev),
            a.meta.block_tables.to(dev), a.meta.context_lens.to(dev)]
+    graphs.q[:b].copy_(ins[0])
+    graphs.k[:b].copy_(ins[1])
+    graphs.v[:b].copy_(ins[2])
+    packed = graphs.pack(b, st.slot_mapping, a.meta.block_tables, a.meta.context_lens,
+                         out=torch.empty((graphs.meta.numel(),), dtype=torch.int32, pin_memory=True))
     store_b, dec_b = decode_bytes(w)
     steps = max(100, min(2000, args.steps // 5))
+
+    def loop(fn, n):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        barrier(world)
+        w0 = time.perf_counter()
+        t0.record()
+        for _ in range(n):
+            fn()
+        t1.record()
+        torch.cuda.synchronize()
+        w1 = time.perf_counter()
+        barrier(world)
+        return t0.elapsed_time(t1) / n, (w0, w1)
+
+    for _ in range(max(3, args.warmup)):
+        graphs.run_packed(b, packed)
+    ms, win = loop(lambda: graphs.run_packed(b, packed), steps)
+    assert kvp.device_status() == 0, "device status after the bucketed loop"
     for _ in range(max(3, args.warmup)):
         graphs.run(*ins)
-    torch.cuda.synchronize()
-    barrier(world)
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    w0 = time.perf_counter()
-    t0.record()
-    for _ in range(steps):
-        graphs.run(*ins)
-    t1.record()
-    torch.cuda.synchronize()
-    w1 = time.perf_counter()
-    barrier(world)
-    assert kvp.device_status() == 0, "device status after the bucketed loop"
-    ms = t0.elapsed_time(t1) / steps
+    ms_copies, _ = loop(lambda: graphs.run(*ins), steps)
+    assert kvp.device_status() == 0, "device status after the bucketed loop (run)"
     bps, ms = aggregate(store_b + dec_b, ms, world)
+    bps_c, ms_copies = aggregate(store_b + dec_b, ms_copies, world)
     del graphs, kc, vc
-    return {"window": (w0, w1), "steps": steps,
+    return {"window": win, "steps": 2 * steps,
             "line": {"workload": "decode B50 padded to the bucket-64 graph, 16/8/128 bs256 NB2048 "
                                  "ctx U[512,4096]", "value": round(bps / 1e9, 2), "unit": "GB/s",
                      "ms_per_step": round(ms, 4), "steps": steps,
-                     "step": "input copies into the graph buffers + replay (attn_decode_paged_append)",
-                     "frac_of_hbm": round(bps / 1e9 / peaks["hbm_gbs"], 4)}}
+                     "step": "one copy of the packed metadata (pinned host -> device) + replay "
+                             "(attn_decode_paged_append); q/k/v in the graph's buffers",
+                     "frac_of_hbm": round(bps / 1e9 / peaks["hbm_gbs"], 4),
+                     "inputs_copied": {"step": "q, k, v, slot_mapping, block_tables, context_lens "
+                                               "copied device -> graph buffers (6 copies, 2 fills) "
+                                               "+ replay", "value": round(bps_c / 1e9, 2),
+                                       "unit": "GB/s", "ms_per_step": round(ms_copies, 4)}}}
 
 
 def measure_decode_large(args, kvp, W, dev, stream, world, peaks):
@@ -699,8 +723,8 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
     one 28-layer graph per batch-size bucket (LayeredDecodeGraphs), as the
     pages' engine does.  Aggregate GB/s over the decode steps (algorithmic
     bytes) and TFLOP/s over the prefill steps (causal FLOPs), each timed by an
-    event pair around the step's 28 layers (for decode: the metadata copies
-    into the graph's buffers and the replay)."""
+    event pair around the step's 28 layers (for decode: the copy of the
+    step's packed metadata into the graph's buffer and the replay)."""
     import torch
     from paged_kv_cache_125_gb300 import engine_trace as E
     from paged_kv_cache_125_gb300.graphs import LayeredDecodeGraphs
@@ -717,6 +741,7 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
     graphs = LayeredDecodeGraphs([(kv[0, l_], kv[1, l_]) for l_ in range(layers)], hq, max_blocks,
                                  max_bs=512, softmax_scale=scale, stream=stream)
     gq = torch.Generator(device=dev).manual_seed(5)
+    meta_len = graphs.meta.numel()
     row = hkv * d * 2
     recs = []
     w0 = time.perf_counter()
@@ -731,15 +756,16 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
             graphs.q[:, :n].copy_(torch.randn((layers, n, hq, d), generator=gq, device=dev))
             graphs.k[:, :n].copy_(torch.randn((layers, n, hkv, d), generator=gq, device=dev))
             graphs.v[:, :n].copy_(torch.randn((layers, n, hkv, d), generator=gq, device=dev))
-        slots = m.slot_mapping.to(dev, non_blocking=True)
         if pre:
+            slots = m.slot_mapping.to(dev, non_blocking=True)
             cq, ck = m.cu_seqlens_q.to(dev, non_blocking=True), m.cu_seqlens_k.to(dev, non_blocking=True)
             bt = None if m.block_tables is None else m.block_tables.to(dev, non_blocking=True)
             ql = (m.cu_seqlens_q[1:] - m.cu_seqlens_q[:-1]).long()
             kl = (m.cu_seqlens_k[1:] - m.cu_seqlens_k[:-1]).long()
             work = 4 * d * hq * int((ql * (kl - ql) + ql * (ql + 1) // 2).sum())
-        else:
-            bt, ctx = m.block_tables.to(dev, non_blocking=True), m.context_lens.to(dev, non_blocking=True)
+        else:  # the step's metadata, packed for its bucket in pinned memory: one copy
+            packed = graphs.pack(n, m.slot_mapping, m.block_tables, m.context_lens,
+                                 out=torch.empty((meta_len,), dtype=torch.int32, pin_memory=True))
             c = m.context_lens.long()
             work = 4 * n * row + int(c.sum()) * row * 2 + 2 * n * hq * d * 2 + \
                 int(((c + bs - 1) // bs).sum()) * 4 + n * 4
@@ -752,7 +778,7 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
                 kvp.attn_prefill_varlen(q, cq, ck, m.max_seqlen_q, m.max_seqlen_k, k=k, v=v, k_cache=kc,
                                         v_cache=vc, block_tables=bt, num_kv_heads=hkv, softmax_scale=scale)
         else:
-            graphs.run(n, slots, bt, ctx)
+            graphs.run_packed(n, packed)
         b.record()
         recs.append((pre, work * layers, a, b))
         sch.postprocess([(7 * i + n) % 151936 for i in ids])
@@ -778,8 +804,9 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
                      "prefill": {"value": round(pre_tf, 2), "unit": "TFLOP/s", "ms": round(pre_ms, 2),
                                  "frac_of_bf16_burst": round(pre_tf / peaks["bf16_tflops"], 4)},
                      "how": "event pair around each step's 28 layers (prefill: kv_store + "
-                            "attn_prefill_varlen, eager; decode: metadata copies + one 28-layer graph "
-                            "replay of attn_decode_paged_append per bucket); "
+                            "attn_prefill_varlen, eager; decode: one copy of the packed metadata from "
+                            "pinned memory + one 28-layer graph replay of attn_decode_paged_append per "
+                            "bucket); "
                             "inputs generated on the device before each step"}}
 
 

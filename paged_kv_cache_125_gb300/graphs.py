@@ -10,6 +10,13 @@ paged decode); the launch configuration depends only on the bucket
 and the fixed capacities, never on the step's data, so one capture serves
 every step.  Padding rows write nothing (slot -1) and read nothing (context
 0), and their output rows are zero.
+
+Step metadata (slot_mapping, context_lens, block_tables) lives in one int32
+buffer whose layout depends on the bucket pb (see ``pack_decode_metadata``):
+each bucket's graph reads its own compact views of it, so a step's metadata,
+padding rows included, arrives in ONE host-to-device copy of a packed pinned
+buffer (``run_packed``).  q, k and v are not part of it: in an engine the
+model's projections write them into the graph's fixed buffers.
 """
 from __future__ import annotations
 
@@ -25,6 +32,82 @@ def default_buckets(max_bs: int) -> list[int]:
     return b
 
 
+def packed_metadata_len(pb: int, width: int) -> int:
+    """int32 entries of the packed metadata of bucket pb."""
+    return pb * (2 + width)
+
+
+def pack_decode_metadata(pb: int, width: int, slot_mapping, block_tables, context_lens, out=None):
+    """Packs the metadata of a decode step of b = len(context_lens) <= pb
+    sequences for the bucket-pb graph: ``[slot_mapping (pb) | context_lens (pb)
+    | block_tables (pb x width)]`` int32, rows b .. pb-1 padded with slot -1,
+    context 0 and block-table entries -1 (block-table columns past the
+    caller's width are -1 as well).  ``out``: an int32 buffer of at least
+    ``packed_metadata_len(pb, width)`` entries (pinned host memory for an
+    asynchronous copy), else a new one on the host.  Returns the packed
+    prefix of ``out``."""
+    import torch
+    b = int(context_lens.shape[0])
+    if b > pb or slot_mapping.shape[0] != b or block_tables.shape[0] != b:
+        raise ValueError("metadata rows must agree and fit the bucket")
+    w = int(block_tables.shape[1])
+    if w > width:
+        raise ValueError("block table wider than the graph's width")
+    n = packed_metadata_len(pb, width)
+    if out is None:
+        out = torch.empty((n,), dtype=torch.int32)
+    buf = out[:n]
+    buf[:pb].fill_(-1)
+    buf[:b].copy_(slot_mapping)
+    buf[pb:2 * pb].zero_()
+    buf[pb:pb + b].copy_(context_lens)
+    bt = buf[2 * pb:].view(pb, width)
+    bt.fill_(-1)
+    bt[:b, :w].copy_(block_tables)
+    return buf
+
+
+class _PackedMeta:
+    """Per-bucket views of one int32 metadata buffer of max_bs x (2 + width)
+    entries; bucket pb's views start at offset 0 in the packed layout."""
+
+    def _init_meta(self, max_bs: int, width: int, dev) -> None:
+        import torch
+        self.width = width
+        self.meta = torch.zeros((packed_metadata_len(max_bs, width),), dtype=torch.int32, device=dev)
+
+    def meta_views(self, pb: int):
+        """(slot_mapping, context_lens, block_tables) that bucket pb's graph reads."""
+        m = self.meta
+        return (m[:pb], m[pb:2 * pb],
+                m[2 * pb:packed_metadata_len(pb, self.width)].view(pb, self.width))
+
+    def _copy_meta(self, b: int, pb: int, slot_mapping, block_tables, context_lens) -> None:
+        slots, ctx, bt = self.meta_views(pb)
+        w = block_tables.shape[1]
+        if w > self.width:
+            raise ValueError("block table wider than max_blocks_per_seq")
+        slots[:b].copy_(slot_mapping)
+        bt[:b, :w].copy_(block_tables)
+        ctx[:b].copy_(context_lens)
+        if pb > b:  # padding rows: write nothing, read nothing
+            slots[b:].fill_(-1)
+            ctx[b:].fill_(0)
+
+    def pack(self, b: int, slot_mapping, block_tables, context_lens, out=None):
+        """Host-side packing of a step's metadata for this object's bucket of b."""
+        return pack_decode_metadata(self.bucket(b), self.width, slot_mapping, block_tables,
+                                    context_lens, out)
+
+    def _load_packed(self, b: int, packed) -> int:
+        pb = self.bucket(b)
+        n = packed_metadata_len(pb, self.width)
+        if packed.dtype != self.meta.dtype or packed.numel() < n:
+            raise ValueError("packed metadata of the wrong type or size for this bucket")
+        self.meta[:n].copy_(packed[:n], non_blocking=True)
+        return pb
+
+
 def bucket_for(buckets: list[int], b: int) -> int:
     """Smallest bucket >= b."""
     for x in buckets:
@@ -33,7 +116,7 @@ def bucket_for(buckets: list[int], b: int) -> int:
     raise ValueError(f"batch of {b} exceeds the largest bucket {buckets[-1]}")
 
 
-class DecodeGraphs:
+class DecodeGraphs(_PackedMeta):
     """Captured store + decode graphs for one layer's cache.
 
     ``k_cache`` / ``v_cache``: [num_blocks, block_size, num_kv_heads, head_dim]
@@ -54,13 +137,11 @@ class DecodeGraphs:
             raise ValueError("a bucket exceeds max_bs")
         self.capacity = max_blocks_per_seq * bs
         self.scale = softmax_scale if softmax_scale is not None else d ** -0.5
-        bf16, i32 = torch.bfloat16, torch.int32
+        bf16 = torch.bfloat16
         self.q = torch.zeros((max_bs, num_heads, d), dtype=bf16, device=dev)
         self.k = torch.zeros((max_bs, hkv, d), dtype=bf16, device=dev)
         self.v = torch.zeros((max_bs, hkv, d), dtype=bf16, device=dev)
-        self.slots = torch.full((max_bs,), -1, dtype=i32, device=dev)
-        self.block_tables = torch.zeros((max_bs, max_blocks_per_seq), dtype=i32, device=dev)
-        self.context_lens = torch.zeros((max_bs,), dtype=i32, device=dev)
+        self._init_meta(max_bs, max_blocks_per_seq, dev)
         self.out = torch.zeros((max_bs, num_heads, d), dtype=bf16, device=dev)
         ws_bytes = attn_decode_workspace_size(max_bs, num_heads, d, self.capacity, bs)
         self.workspace = torch.empty((max(ws_bytes, 1),), dtype=torch.uint8, device=dev)
@@ -70,10 +151,10 @@ class DecodeGraphs:
             self.graphs[b] = self._capture(b)
 
     def _step(self, b: int) -> None:
-        attn_decode_paged_append(self.q[:b], self.k[:b], self.v[:b], self.slots[:b], self.k_cache,
-                                 self.v_cache, self.block_tables[:b], self.context_lens[:b],
-                                 self.capacity, softmax_scale=self.scale, workspace=self.workspace,
-                                 out=self.out[:b])
+        slots, ctx, bt = self.meta_views(b)
+        attn_decode_paged_append(self.q[:b], self.k[:b], self.v[:b], slots, self.k_cache,
+                                 self.v_cache, bt, ctx, self.capacity, softmax_scale=self.scale,
+                                 workspace=self.workspace, out=self.out[:b])
 
     def _capture(self, b: int):
         import torch
@@ -96,26 +177,28 @@ class DecodeGraphs:
         Returns a view of the first b output rows (valid until the next run)."""
         b = q.shape[0]
         pb = self.bucket(b)
-        w = block_tables.shape[1]
-        if w > self.block_tables.shape[1]:
-            raise ValueError("block table wider than max_blocks_per_seq")
         # No host read of context_lens (that would synchronise every step): a
         # context above the capacity is caught by the kernel, which skips the
         # row and sets KVP_ERR_DEVICE_DATA in the device status.
         self.q[:b].copy_(q)
         self.k[:b].copy_(k)
         self.v[:b].copy_(v)
-        self.slots[:b].copy_(slot_mapping)
-        self.block_tables[:b, :w].copy_(block_tables)
-        self.context_lens[:b].copy_(context_lens)
-        if pb > b:  # padding rows: write nothing, read nothing
-            self.slots[b:pb].fill_(-1)
-            self.context_lens[b:pb].fill_(0)
+        self._copy_meta(b, pb, slot_mapping, block_tables, context_lens)
+        self.graphs[pb].replay()
+        return self.out[:b]
+
+    def run_packed(self, b: int, packed):
+        """One decode step of b sequences whose new rows the caller has written
+        into q/k/v[:b], with the step's metadata packed for bucket(b) by
+        ``pack`` (one copy; from pinned host memory it is asynchronous, and the
+        caller keeps the buffer unchanged until the copy has run).  Returns a
+        view of the first b output rows (valid until the next run)."""
+        pb = self._load_packed(b, packed)
         self.graphs[pb].replay()
         return self.out[:b]
 
 
-class LayeredDecodeGraphs:
+class LayeredDecodeGraphs(_PackedMeta):
     """The decode step of a whole model as one graph per bucket: every layer's
     ``attn_decode_paged_append`` in one capture, the way the pages' engine
     captures its model forward for decode ("nano-vLLM-1", ModelRunner
@@ -142,25 +225,24 @@ class LayeredDecodeGraphs:
             raise ValueError("a bucket exceeds max_bs")
         self.capacity = max_blocks_per_seq * bs
         self.scale = softmax_scale if softmax_scale is not None else d ** -0.5
-        bf16, i32 = torch.bfloat16, torch.int32
+        bf16 = torch.bfloat16
         self.q = torch.zeros((n_layers, max_bs, num_heads, d), dtype=bf16, device=dev)
         self.k = torch.zeros((n_layers, max_bs, hkv, d), dtype=bf16, device=dev)
         self.v = torch.zeros((n_layers, max_bs, hkv, d), dtype=bf16, device=dev)
         self.out = torch.zeros((n_layers, max_bs, num_heads, d), dtype=bf16, device=dev)
-        self.slots = torch.full((max_bs,), -1, dtype=i32, device=dev)
-        self.block_tables = torch.zeros((max_bs, max_blocks_per_seq), dtype=i32, device=dev)
-        self.context_lens = torch.zeros((max_bs,), dtype=i32, device=dev)
+        self._init_meta(max_bs, max_blocks_per_seq, dev)
         ws_bytes = attn_decode_workspace_size(max_bs, num_heads, d, self.capacity, bs)
         self.workspace = torch.empty((max(ws_bytes, 1),), dtype=torch.uint8, device=dev)
         self.stream = stream or torch.cuda.Stream(dev)
         self.graphs = {b: self._capture(b) for b in self.buckets}
 
     def _step(self, b: int) -> None:
+        slots, ctx, bt = self.meta_views(b)
         for layer, (kc, vc) in enumerate(self.kv_layers):
             attn_decode_paged_append(self.q[layer, :b], self.k[layer, :b], self.v[layer, :b],
-                                     self.slots[:b], kc, vc, self.block_tables[:b],
-                                     self.context_lens[:b], self.capacity, softmax_scale=self.scale,
-                                     workspace=self.workspace, out=self.out[layer, :b])
+                                     slots, kc, vc, bt, ctx, self.capacity,
+                                     softmax_scale=self.scale, workspace=self.workspace,
+                                     out=self.out[layer, :b])
 
     def _capture(self, b: int):
         import torch
@@ -181,14 +263,13 @@ class LayeredDecodeGraphs:
         """One decode step of b sequences whose new rows the caller has written
         into q/k/v[:, :b]; returns the bucket replayed (outputs in out[:, :b])."""
         pb = self.bucket(b)
-        w = block_tables.shape[1]
-        if w > self.block_tables.shape[1]:
-            raise ValueError("block table wider than max_blocks_per_seq")
-        self.slots[:b].copy_(slot_mapping)
-        self.block_tables[:b, :w].copy_(block_tables)
-        self.context_lens[:b].copy_(context_lens)
-        if pb > b:  # padding rows: write nothing, read nothing
-            self.slots[b:pb].fill_(-1)
-            self.context_lens[b:pb].fill_(0)
+        self._copy_meta(b, pb, slot_mapping, block_tables, context_lens)
+        self.graphs[pb].replay()
+        return pb
+
+    def run_packed(self, b: int, packed) -> int:
+        """As ``run``, with the metadata packed for bucket(b) by ``pack`` and
+        loaded in one copy; returns the bucket replayed."""
+        pb = self._load_packed(b, packed)
         self.graphs[pb].replay()
         return pb

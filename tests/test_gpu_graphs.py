@@ -39,6 +39,20 @@ def test_bucketed_graph_decode_matches_oracle(hq, hkv, d, bs):
         # padding rows of the bucket produced zeros and wrote nothing
         pb = graphs.bucket(b)
         assert torch.all(graphs.out[b:pb].float() == 0)
+        # The same step with its metadata packed for the bucket in pinned
+        # memory, one copy (q/k/v already in the graph's buffers): the same
+        # bits, and the cache rows stored again unchanged.
+        first = out.clone()
+        packed = graphs.pack(b, st.slot_mapping, m.block_tables, m.context_lens,
+                             out=torch.empty((graphs.meta.numel(),), dtype=torch.int32,
+                                             pin_memory=True))
+        graphs.out.fill_(float("nan"))
+        out2 = graphs.run_packed(b, packed)
+        torch.cuda.synchronize()
+        assert_status_ok()
+        assert torch.equal(out2.view(torch.int16), first.view(torch.int16)), b
+        assert torch.all(graphs.out[b:pb].float() == 0)
+        assert np.array_equal(u16(kc), kr) and np.array_equal(u16(vc), vr), b
 
 
 def test_layered_graph_decode_matches_oracle():
@@ -79,3 +93,11 @@ def test_layered_graph_decode_matches_oracle():
             ref = oracle.decode(qs[layer], kr, vr, a.meta.block_tables, a.meta.context_lens, hq, hkv,
                                 w.scale)
             assert_attn_close(graphs.out[layer, :b], ref, f"layered decode b={b} layer {layer}")
+        # the packed-metadata path replays the same bucket and gives the same bits
+        first = graphs.out[:, :b].clone()
+        graphs.out.fill_(float("nan"))
+        packed = graphs.pack(b, st.slot_mapping, a.meta.block_tables, a.meta.context_lens)
+        assert graphs.run_packed(b, packed.pin_memory()) == pb
+        torch.cuda.synchronize()
+        assert_status_ok()
+        assert torch.equal(graphs.out[:, :b].view(torch.int16), first.view(torch.int16)), b
