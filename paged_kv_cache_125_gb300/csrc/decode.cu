@@ -47,7 +47,8 @@ namespace kvp {
 namespace {
 
 constexpr int kBaseWarps = 8;  // consumer warps before the head split
-constexpr int kStages = 6;
+constexpr int kStages = 6;  // ring depth (one less where the CTA would not fit, see ring_stages)
+constexpr size_t kSmemPerCta = 227 * 1024;
 
 // Query heads of a kv head are split over HS warps when a warp holding all
 // G of them would need G * D / 8 query floats plus as many accumulators per
@@ -150,19 +151,28 @@ __host__ __device__ constexpr bool q_in_smem() {
 }
 
 template <int D, int G>
-__host__ __device__ constexpr size_t decode_smem_bytes() {
+__host__ __device__ constexpr size_t decode_smem_bytes(int ns) {
   constexpr int HS = head_split<D, G>(), CW = consumer_warps<HS>(), GE = G / HS;
-  return 2 * kStages * stage_half_bytes<D>() + kStages * sizeof(StageMeta) +
-         (2 * kStages + 2 * CW) * sizeof(uint64_t) + (size_t)CW * GE * (D + 2) * sizeof(float) +
+  return 2 * ns * stage_half_bytes<D>() + ns * sizeof(StageMeta) +
+         (2 * ns + 2 * CW) * sizeof(uint64_t) + (size_t)CW * GE * (D + 2) * sizeof(float) +
          (q_in_smem<D, GE>() ? (size_t)CW * GE * D * sizeof(float) : 0);
 }
+
+// Stages of the K/V ring: kStages, or one less where the head split's query
+// and partial staging would take the CTA past 227 KiB (G * D = 1024: eight
+// query heads per kv head at head_dim 128).
+template <int D, int G>
+__host__ __device__ constexpr int ring_stages() {
+  return decode_smem_bytes<D, G>(kStages) <= kSmemPerCta ? kStages : kStages - 1;
+}
+static_assert(decode_smem_bytes<128, 8>(ring_stages<128, 8>()) <= kSmemPerCta, "decode CTA smem");
 
 // ---------------------------------------------------------------- producer
 
 // Stage loop of the producer (one thread): copies the CTA's token range
 // [start, end), first sequence b0 starting at token cum0 of the batch, into
 // the ring, then posts the end marker.
-template <int D>
+template <int D, int RS>
 __device__ void stream_stages(const DecodeArgs& a, const AppendArgs& app, uint8_t* ringK,
                               uint8_t* ringV, StageMeta* meta, uint64_t* full, uint64_t* empty,
                               long long start, long long end, int b0, long long cum0, int cap) {
@@ -231,7 +241,7 @@ __device__ void stream_stages(const DecodeArgs& a, const AppendArgs& app, uint8_
       issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
       first = false;
       t += n;
-      if (++s == kStages) {
+      if (++s == RS) {
         s = 0;
         ph ^= 1u;
       }
@@ -247,7 +257,7 @@ __device__ void stream_stages(const DecodeArgs& a, const AppendArgs& app, uint8_
     return;
   }
   // A wait expired: let every copy this CTA issued land before the CTA exits.
-  for (int i = 0; i < kStages; ++i)
+  for (int i = 0; i < RS; ++i)
     if (issued >> i & 1u) mbar_wait(&full[i], issued_ph >> i & 1u, a.status);
 }
 
@@ -285,7 +295,7 @@ __device__ void fused_store(const DecodeArgs& a, const AppendArgs& app, int lane
   }
 }
 
-template <int D>
+template <int D, int RS>
 __device__ void decode_producer(const DecodeArgs& a, const AppendArgs& app, uint8_t* ringK,
                                 uint8_t* ringV, StageMeta* meta, uint64_t* full, uint64_t* empty) {
   const int lane = threadIdx.x & 31;
@@ -337,7 +347,7 @@ __device__ void decode_producer(const DecodeArgs& a, const AppendArgs& app, uint
     }
   }
   if (lane == 0)
-    stream_stages<D>(a, app, ringK, ringV, meta, full, empty, start, end, b0, cum0, cap);
+    stream_stages<D, RS>(a, app, ringK, ringV, meta, full, empty, start, end, b0, cum0, cap);
   // The fused store, by the whole warp once every stage is issued: it overlaps
   // the consumers' last stages instead of delaying the first copies.
   __syncwarp();
@@ -348,7 +358,7 @@ __device__ void decode_producer(const DecodeArgs& a, const AppendArgs& app, uint
 
 // Template G here is the number of query heads this warp owns (the group
 // size divided by the head split HS); hs selects which part of the group.
-template <int D, int G, int HS>
+template <int D, int G, int HS, int RS>
 __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const uint8_t* ringV,
                                 const StageMeta* meta, uint64_t* full, uint64_t* empty,
                                 uint64_t* xfull, uint64_t* xfree, float* xw, float* qs_all) {
@@ -574,7 +584,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
 
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);
-    if (++s == kStages) {
+    if (++s == RS) {
       s = 0;
       ph ^= 1u;
     }
@@ -703,14 +713,14 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
 template <int D, int G, int HS>
 __global__ void __maxnreg__(HS == 1 ? 168 : kSplitLaunchRegs) decode_split_kernel(const DecodeArgs a,
                                                                 const AppendArgs app) {
-  constexpr int CW = consumer_warps<HS>(), GE = G / HS;
+  constexpr int CW = consumer_warps<HS>(), GE = G / HS, RS = ring_stages<D, G>();
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ringK = smem;
-  uint8_t* ringV = smem + kStages * stage_half_bytes<D>();
-  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + 2 * kStages * stage_half_bytes<D>());
-  uint64_t* full = reinterpret_cast<uint64_t*>(meta + kStages);
-  uint64_t* empty = full + kStages;
-  uint64_t* xfull = empty + kStages;
+  uint8_t* ringV = smem + RS * stage_half_bytes<D>();
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + 2 * RS * stage_half_bytes<D>());
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + RS);
+  uint64_t* empty = full + RS;
+  uint64_t* xfull = empty + RS;
   uint64_t* xfree = xfull + CW;
   float* xw = reinterpret_cast<float*>(xfree + CW);
   float* qs = xw + (size_t)CW * GE * (D + 2);
@@ -718,7 +728,7 @@ __global__ void __maxnreg__(HS == 1 ? 168 : kSplitLaunchRegs) decode_split_kerne
   if (threadIdx.x == 0) {
     // The merge kernel may be scheduled now; it waits for this grid to finish.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < RS; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], CW);
     }
@@ -733,16 +743,16 @@ __global__ void __maxnreg__(HS == 1 ? 168 : kSplitLaunchRegs) decode_split_kerne
   const int warp = threadIdx.x >> 5;
   if constexpr (HS == 1) {
     if (warp == CW)
-      decode_producer<D>(a, app, ringK, ringV, meta, full, empty);
+      decode_producer<D, RS>(a, app, ringK, ringV, meta, full, empty);
     else
-      decode_consumer<D, GE, HS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
+      decode_consumer<D, GE, HS, RS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
   } else {
     if (warp >= CW) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSplitProducerRegs));
-      if (warp == CW) decode_producer<D>(a, app, ringK, ringV, meta, full, empty);
+      if (warp == CW) decode_producer<D, RS>(a, app, ringK, ringV, meta, full, empty);
     } else {
       asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSplitConsumerRegs));
-      decode_consumer<D, GE, HS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
+      decode_consumer<D, GE, HS, RS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
     }
   }
 }
@@ -823,7 +833,7 @@ template <int D, int G>
 cudaError_t launch_decode_t(const DecodeArgs& a, const AppendArgs& app, int ctas,
                             cudaStream_t stream) {
   constexpr int HS = head_split<D, G>();
-  const size_t smem = decode_smem_bytes<D, G>();
+  const size_t smem = decode_smem_bytes<D, G>(ring_stages<D, G>());
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, HS>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -851,8 +861,7 @@ bool decode_supported(int num_heads, int num_kv_heads, int head_dim) {
   if (num_kv_heads != 1 && num_kv_heads != 2 && num_kv_heads != 4 && num_kv_heads != 8)
     return false;
   const int G = num_heads / num_kv_heads;
-  if (head_dim == 128) return G == 1 || G == 2 || G == 4;
-  if (head_dim == 64) return G == 1 || G == 2 || G == 4 || G == 8;
+  if (head_dim == 128 || head_dim == 64) return G == 1 || G == 2 || G == 4 || G == 8;
   return false;
 }
 
@@ -913,6 +922,7 @@ cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k
       case 1: return launch_decode_t<128, 1>(a, ap, plan.ctas, stream);
       case 2: return launch_decode_t<128, 2>(a, ap, plan.ctas, stream);
       case 4: return launch_decode_t<128, 4>(a, ap, plan.ctas, stream);
+      case 8: return launch_decode_t<128, 8>(a, ap, plan.ctas, stream);
     }
   } else if (head_dim == 64) {
     switch (G) {

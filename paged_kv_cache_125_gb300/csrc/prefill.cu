@@ -307,8 +307,8 @@ __device__ void build_order(const PrefillArgs& a, Sched* sc) {
 // against the value last seen, repeated against the value it returns until
 // the slot carries this epoch (whichever CTA's CAS lands first does it; an
 // increment that lands after it is already a position of this launch).
-// Positions stay below 2^15 (at most kMaxPairs x 8 items); 0x3fffffff means
-// none (an error was recorded).
+// Positions are below kMaxPairs x num_kv_heads; 0x3fffffff means none (an
+// error was recorded).
 __device__ __forceinline__ int queue_fetch(const PrefillArgs& a) {
   unsigned long long v = atomicAdd(a.qslot, 1ull);
   if ((uint32_t)(v >> 32) == a.epoch) return (int)(v & 0xffffffffull);

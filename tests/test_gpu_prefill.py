@@ -59,6 +59,43 @@ def test_prefill_shapes(hq, hkv, d, bs, lens, cached):
     _check(w)
 
 
+def _schedule_case(kind):
+    rng = np.random.default_rng({"cu_global": 1, "cu_global_rr": 2, "at_limit": 3, "over_limit": 4}[kind])
+    if kind == "cu_global":  # 530 short prompts: cu_seqlens stay in global memory, cost order kept
+        hq, hkv, d, bs = 4, 2, 128, 16
+        lens = rng.integers(1, 101, size=530).tolist()
+    elif kind == "cu_global_rr":  # 600 prompts, one long: global cu_seqlens and round-robin order
+        hq, hkv, d, bs = 8, 2, 64, 32
+        lens = rng.integers(1, 41, size=599).tolist() + [1500]
+    else:  # 64 (at the limit) or 65 (past it) prompts, one of 4096 tokens: 64 pair ranks each
+        hq, hkv, d, bs = 4, 1, 64, 64
+        n = 64 if kind == "at_limit" else 65
+        lens = [4096] + rng.integers(1, 201, size=n - 1).tolist()
+    cached = [int(rng.integers(0, (L - 1) // bs + 1)) if L > bs and rng.random() < 0.5 else 0
+              for L in lens]
+    nb = sum(W.num_blocks_for(L, bs) for L in lens) + 3
+    return W.prefill_workload(f"sched_{kind}", lens, cached, hq, hkv, d, bs, nb)
+
+
+@pytest.mark.parametrize("kind,dynamic,cu_in_smem", [("cu_global", True, False),
+                                                     ("cu_global_rr", False, False),
+                                                     ("at_limit", True, True),
+                                                     ("over_limit", False, True)])
+def test_prefill_schedule_capacity_fallbacks(kind, dynamic, cu_in_smem):
+    """The per-CTA schedule holds cu_seqlens for at most 519 sequences and
+    the cost order for at most 4096 (pair rank, sequence) entries; past them
+    the kernel reads cu_seqlens from global memory and takes items
+    round-robin.  Each side of both limits against the oracle."""
+    w = _schedule_case(kind)
+    m = w.steps[0].attn.meta
+    g = w.num_heads // w.num_kv_heads
+    num_seqs = m.cu_seqlens_q.numel() - 1
+    max_pairs = -(-m.max_seqlen_q // (2 * (128 // g)))
+    assert (max_pairs * num_seqs <= 4096) == dynamic
+    assert (num_seqs + 1 <= 520) == cu_in_smem
+    _check(w)
+
+
 def test_prefill_fully_cached_prompt_has_no_rows():
     """A block-aligned prompt whose every block hit the prefix cache has
     q_len 0; the other sequences are unaffected."""

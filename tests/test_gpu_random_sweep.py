@@ -16,8 +16,7 @@ def _random_case(seed):
     rng = np.random.default_rng(1000 + seed)
     hkv = int(rng.choice([1, 2, 4, 8]))
     d = int(rng.choice([64, 128]))
-    groups = [1, 2, 4] if d == 128 else [1, 2, 4, 8]
-    g = int(rng.choice(groups))
+    g = int(rng.choice([1, 2, 4, 8]))
     bs = int(rng.choice([16, 32, 64, 128, 256]))
     nseq = int(rng.integers(1, 7))
     lens, cached = [], []

@@ -105,6 +105,8 @@ def test_decode_config2_full_size():
     (8, 2, 64, 16, [300, 301]),
     (8, 1, 64, 64, [1000]),
     (4, 1, 128, 16, [70, 15]),
+    (64, 8, 128, 256, [3000, 1, 255, 257]),                      # G=8 at head_dim 128
+    (16, 2, 128, 32, [700, 33]),
 ])
 def test_decode_shapes_and_ragged_lengths(hq, hkv, d, bs, lens):
     nb = sum(W.num_blocks_for(L, bs) for L in lens) + 7
@@ -216,6 +218,7 @@ def test_decode_append_config2_full_size():
     (32, 8, 128, 256, [8192, 128, 4096]),
     (4, 2, 128, 48, [47, 48, 49, 2000]),
     (8, 1, 64, 64, [1000]),
+    (64, 8, 128, 256, [3000, 1, 255, 257]),
 ])
 def test_decode_append_shapes_and_ragged_lengths(hq, hkv, d, bs, lens):
     """New rows at the first slot of a block (stage of one token), mid-block and
