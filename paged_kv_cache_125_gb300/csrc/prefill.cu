@@ -39,7 +39,10 @@
 //           stale reference), writes P as bf16 pairs over the first 64
 //           columns of its S region, and at the end of an item normalises O
 //           and stores bf16.  The warpgroup of an item's last tile releases
-//           the K, V and Q slots once it sees the S that last read them.
+//           the K and Q slots once it sees the S that last read them; a V
+//           slot is released by a commit of the MMA thread right after the
+//           last PV that reads it (it would otherwise wait for the next S,
+//           another batch of MMAs later).
 // Synchronisation facts the design relies on: a tcgen05.commit arrives only
 // when every earlier MMA of the issuing thread has completed, so the commit
 // after S_X(j+1) also says PV_X(j) is done (O_X may be rescaled, and P_X's
@@ -571,6 +574,7 @@ __device__ void mma_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, ui
             goto drain;
           tc_fence_after();
           mma_pv<D>(tbase + (2 + x) * kBN, tbase + x * kBN, dv0 + st * kSlotStep, j > 0);
+          if (x == ntile - 1) umma_commit(&bars[B_VEMPTY + st]);  // last reader of V(j)
           if (more) {
             mma_qk<D>(tbase + x * kBN, dq0 + x * kQStep, dk0 + (jn & 1) * kSlotStep);
             umma_commit(&bars[B_SFULL + x]);
@@ -639,9 +643,9 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
   uint32_t ns = 0;    // S tiles consumed by this tile's warpgroup
   uint32_t nit = 0;   // items this warpgroup took part in
   uint32_t jt0 = 0;   // kv tiles of all earlier items (ring slot of tile j = (jt0 + j) & 1)
-  // The warpgroup of an item's last query tile releases the K, V and Q slots:
-  // it observes S of that tile complete, and that MMA was issued after every
-  // earlier MMA that read those slots.
+  // The warpgroup of an item's last query tile releases the K and Q slots: it
+  // observes S of that tile complete, and that MMA was issued after every
+  // earlier MMA that read those slots.  (V slots: MMA commits.)
   const bool releaser = (warp & 3) == 0 && lane == 0;
   Item it;
   for (int k = 0; ring_item(sc, bars, k, it, true, a.status); ++k, jt0 += it.n_tiles) {
@@ -657,9 +661,8 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
     for (int j = 0; j < it.n_tiles; ++j) {
       if (!mbar_wait(&bars[B_SFULL + x], ns & 1, a.status)) return;
       ++ns;
-      if (last && releaser) {  // S(j) done: K(j) free; PV(j-1) done: V(j-1) free
+      if (last && releaser) {  // S(j) done: K(j) free
         mbar_arrive(&bars[B_KEMPTY + ((jt0 + j) & 1)]);
-        if (j > 0) mbar_arrive(&bars[B_VEMPTY + ((jt0 + j - 1) & 1)]);
         if (j + 1 == it.n_tiles) mbar_arrive(&bars[B_QEMPTY]);
       }
       tc_fence_after();
@@ -746,7 +749,6 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
     // Epilogue: wait for this tile's last PV, O / l -> bf16 -> out.
     if (!mbar_wait(&bars[B_PVDONE + x], nit & 1, a.status)) return;
     ++nit;
-    if (last && releaser) mbar_arrive(&bars[B_VEMPTY + ((jt0 + it.n_tiles - 1) & 1)]);
     tc_fence_after();
     uint32_t ov[D / 32][32];
 #pragma unroll
