@@ -53,12 +53,12 @@ N_SETS = 4
 TRAFFIC = {
     # decode B64 workload (one input set), one ncu --set full capture of the split kernel
     "decode": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu",
-               "sha256": "433d40b20eb179859e88382bab3348e25d4f55996ec0a81e4422bd574c42a5b1",
-               "bytes": 569290240 + 4349696},
+               "sha256": "6714505f9679338af3c493ee75631c3e57932872a7e33bd5287ac720069b22d3",
+               "bytes": 569288960 + 4451072},
     # prefill workload (8 prompts, 32/8/128), one ncu --set full capture
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
-                "sha256": "623ae671c1bc988ce2deebe20b6ecd547d5163ebdd114e0aec295b18e99cf2d9",
-                "bytes": 124200192 + 34861312},
+                "sha256": "7202843ebee04788acca15514bba8b861c474cba85d4a42595a64edce6a83eb4",
+                "bytes": 124059136 + 34817536},
 }
 
 
