@@ -79,6 +79,16 @@ int kvp_version(void);
  * itself failed. */
 int kvp_device_status(void);
 
+/* Self-test of the bounded-wait failure path (no fault, no hang): launches one
+ * thread on `stream` that waits on a shared-memory mbarrier through the wait
+ * every kernel uses, with a 2 ms limit instead of the kernels' 2 s.
+ *   arrive = 0  nothing arrives: the wait expires, KVP_ERR_DEVICE_TIMEOUT is
+ *               recorded in the device status word, the kernel returns.
+ *   arrive != 0 the thread arrives first: the wait succeeds, nothing recorded.
+ * Returns KVP_OK once launched, or KVP_ERR_CUDA.  Read the outcome with
+ * kvp_device_status() after the stream has finished. */
+int kvp_selftest_wait(int arrive, kvp_stream_t stream);
+
 /*
  * kv_store - slot-mapped scatter of the step's new K/V rows.
  *

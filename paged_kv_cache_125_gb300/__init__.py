@@ -21,7 +21,7 @@ import threading
 
 __all__ = ["kv_store", "kv_copy_blocks", "attn_prefill_varlen", "attn_decode_paged", "attn_decode_workspace_size",
            "attn_decode_paged_noalloc", "attn_decode_paged_append",
-           "device_status", "library", "library_path", "KvpError"]
+           "device_status", "selftest_wait", "library", "library_path", "KvpError"]
 
 _LIB_LOCK = threading.Lock()
 _LIB = None
@@ -36,6 +36,7 @@ SIGNATURES = {
     "kvp_last_error": (ctypes.c_char_p, []),
     "kvp_version": (_I32, []),
     "kvp_device_status": (_I32, []),
+    "kvp_selftest_wait": (_I32, [_I32, _P]),
     "kv_store": (_I32, [_P, _P, _I64, _I64, _P, _I64, _P, _P, _I64, _I32, _I32, _I32, _P]),
     "kv_copy_blocks": (_I32, [_P, _I64, _I64, _I64, _I64, _P, _I64, _P]),
     "attn_prefill_varlen": (_I32, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _I64, _I32, _P, _I32,
@@ -130,6 +131,16 @@ def _cache_dims(k_cache, v_cache):
 def device_status() -> int:
     """Reads and clears the device status word (synchronizes)."""
     return int(library().kvp_device_status())
+
+
+def selftest_wait(arrive: bool, stream=None) -> None:
+    """Launches the bounded-wait self-test on the current device: one thread
+    waits 2 ms at most on a barrier that it arrives on first (arrive=True) or
+    that nothing arrives on (the wait expires and KVP_ERR_DEVICE_TIMEOUT is
+    recorded).  Read the outcome with device_status()."""
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    _check(library().kvp_selftest_wait(1 if arrive else 0, ctypes.c_void_p(s.cuda_stream)))
 
 
 def kv_store(k, v, slot_mapping, k_cache, v_cache) -> None:

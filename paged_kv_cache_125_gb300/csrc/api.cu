@@ -93,6 +93,15 @@ int kvp_device_status(void) {
   return value;
 }
 
+int kvp_selftest_wait(int arrive, kvp_stream_t stream) {
+  int dev, *status, sms;
+  int rc = device_info(&dev, &status, &sms);
+  if (rc) return rc;
+  cudaError_t e = kvp::launch_selftest_wait(arrive, status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail_cuda(e, "kvp_selftest_wait launch");
+  return KVP_OK;
+}
+
 int kv_store(const kvp_bf16* k, const kvp_bf16* v, int64_t k_stride_tok, int64_t v_stride_tok,
              const int32_t* slot_mapping, int64_t num_tokens, kvp_bf16* k_cache,
              kvp_bf16* v_cache, int64_t num_blocks, int block_size, int num_kv_heads,

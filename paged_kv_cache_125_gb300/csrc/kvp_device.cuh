@@ -68,7 +68,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// records KVP_ERR_DEVICE_TIMEOUT) if it has not completed after kWaitLimitNs.
+// records KVP_ERR_DEVICE_TIMEOUT) if it has not completed after kLimitNs
+// (every kernel uses the default; the wait self-test a shorter limit).
+template <unsigned long long kLimitNs = kWaitLimitNs>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
@@ -76,7 +78,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > kLimitNs) {
       record_error(status, KVP_ERR_DEVICE_TIMEOUT);
       return false;
     }

@@ -13,6 +13,10 @@ namespace kvp {
 // api.cu: records the calling thread's message for kvp_last_error(); returns code.
 int set_last_error(int code, const char* fmt, ...);
 
+// selftest.cu: one thread waits on a barrier (arrive: after arriving on it
+// itself; else nothing arrives and the 2 ms wait expires).
+cudaError_t launch_selftest_wait(int arrive, int* status, cudaStream_t stream);
+
 // kv_store.cu
 cudaError_t launch_kv_store(const uint16_t* k, const uint16_t* v, int64_t k_stride,
                             int64_t v_stride, const int32_t* slots, int64_t n, uint16_t* k_cache,
