@@ -57,7 +57,13 @@ class NativeScheduler:
         self.block_size = block_size
         self.max_num_seqs = max_num_seqs
         self._ids = np.zeros(max_num_seqs, dtype=np.int64)
+        self._ids_addr = self._ids.ctypes.data
         self._n = 0
+        # out-parameters of the per-step calls, made once
+        self._pre, self._t, self._mb = ctypes.c_int(), ctypes.c_int64(), ctypes.c_int()
+        self._mq, self._mk, self._hp = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        self._refs = [ctypes.byref(x) for x in (self._pre, self._t, self._mb, self._mq, self._mk,
+                                                 self._hp)]
 
     def close(self):
         if self._h:
@@ -92,36 +98,40 @@ class NativeScheduler:
                 "block_table": table[:ne.value].tolist()}
 
     def step(self):
-        """Schedules one step -> (seq_ids, is_prefill, metadata)."""
-        pre = ctypes.c_int()
-        n = self._lib.kvp_sched_schedule(self._h, _p(self._ids), ctypes.byref(pre))
+        """Schedules one step -> (seq_ids, is_prefill, metadata).  The int32
+        metadata of a step shares one fresh buffer (the library fills every
+        entry), so a step passes the library two addresses."""
+        lib, h, r = self._lib, self._h, self._refs
+        n = lib.kvp_sched_schedule(h, self._ids_addr, r[0])
         _check(min(n, 0))
         self._n = n
-        t, mb = ctypes.c_int64(), ctypes.c_int()
-        _check(self._lib.kvp_sched_step_sizes(self._h, ctypes.byref(t), ctypes.byref(mb)))
-        T, MB = t.value, max(mb.value, 1)
-        pos = np.zeros(T, dtype=np.int64)
-        slots = np.zeros(T, dtype=np.int32)
-        tables = np.zeros((n, MB), dtype=np.int32)
+        _check(lib.kvp_sched_step_sizes(h, r[1], r[2]))
+        T, MB = self._t.value, max(self._mb.value, 1)
         ids = self._ids[:n].tolist()
-        if pre.value:
-            cq = np.zeros(n + 1, dtype=np.int32)
-            ck = np.zeros(n + 1, dtype=np.int32)
-            mq, mk, hp = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
-            _check(self._lib.kvp_sched_prepare(self._h, _p(cq), _p(ck), _p(pos), _p(slots), None,
-                                               _p(tables), MB, ctypes.byref(mq), ctypes.byref(mk),
-                                               ctypes.byref(hp)))
-            meta = PrefillMeta(torch.from_numpy(cq), torch.from_numpy(ck), mq.value, mk.value,
-                               torch.from_numpy(pos), torch.from_numpy(slots),
-                               torch.from_numpy(tables) if hp.value else None)
+        pos = np.empty(T, dtype=np.int64)
+        if self._pre.value:
+            # [cu_q (n+1) | cu_k (n+1) | slots (T) | block tables (n x MB)]
+            o1, o2, o3 = n + 1, 2 * (n + 1), 2 * (n + 1) + T
+            buf = np.empty(o3 + n * MB, dtype=np.int32)
+            b = buf.ctypes.data
+            _check(lib.kvp_sched_prepare(h, b, b + 4 * o1, pos.ctypes.data, b + 4 * o2, None,
+                                         b + 4 * o3, MB, r[3], r[4], r[5]))
+            meta = PrefillMeta(torch.from_numpy(buf[:o1]), torch.from_numpy(buf[o1:o2]),
+                               self._mq.value, self._mk.value, torch.from_numpy(pos),
+                               torch.from_numpy(buf[o2:o3]),
+                               torch.from_numpy(buf[o3:].reshape(n, MB)) if self._hp.value else None)
         else:
-            ctx = np.zeros(n, dtype=np.int32)
-            _check(self._lib.kvp_sched_prepare(self._h, None, None, _p(pos), _p(slots), _p(ctx),
-                                               _p(tables), MB, None, None, None))
-            meta = DecodeMeta(torch.from_numpy(pos), torch.from_numpy(ctx), torch.from_numpy(slots),
-                              torch.from_numpy(tables), int(ctx.max()))
-        return ids, bool(pre.value), meta
+            # [context_lens (n) | slots (n) | block tables (n x MB)]
+            buf = np.empty(2 * n + n * MB, dtype=np.int32)
+            b = buf.ctypes.data
+            _check(lib.kvp_sched_prepare(h, None, None, pos.ctypes.data, b + 4 * n, b, b + 8 * n,
+                                         MB, None, None, None))
+            ctx = buf[:n]
+            meta = DecodeMeta(torch.from_numpy(pos), torch.from_numpy(ctx),
+                              torch.from_numpy(buf[n:2 * n]),
+                              torch.from_numpy(buf[2 * n:].reshape(n, MB)), int(ctx.max()))
+        return ids, bool(self._pre.value), meta
 
     def postprocess(self, token_ids) -> None:
         t = np.ascontiguousarray(token_ids, dtype=np.int64)
-        _check(self._lib.kvp_sched_postprocess(self._h, _p(t), t.shape[0]))
+        _check(self._lib.kvp_sched_postprocess(self._h, t.ctypes.data, t.shape[0]))
