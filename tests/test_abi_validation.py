@@ -116,3 +116,42 @@ def test_prefill_validation(lib):
     assert _prefill(lib, bt=None, **live) == INVALID and "packed" in _err(lib)  # no k / v
     assert _prefill(lib, bt=None, k=A, v=A, kv_stride=8 * 128 + 4, **live) == INVALID
     assert _prefill(lib, q=MIS, **live) == INVALID and "alignment" in _err(lib)
+
+
+def _copy(lib, **kw):
+    a = dict(cache=A, planes=56, stride=160 * 256 * 8 * 128, nb=160, be=256 * 8 * 128, m=A, n=0)
+    a.update(kw)
+    return lib.kv_copy_blocks(a["cache"], a["planes"], a["stride"], a["nb"], a["be"], a["m"], a["n"],
+                              None)
+
+
+def test_copy_blocks_validation(lib):
+    assert _copy(lib) == OK  # no pairs
+    assert _copy(lib, n=-1) == INVALID and "num_pairs" in _err(lib)
+    assert _copy(lib, planes=0) == INVALID and "shape" in _err(lib)
+    assert _copy(lib, stride=160 * 256 * 8 * 128 - 1) == INVALID and "plane_stride" in _err(lib)
+    assert _copy(lib, n=3, m=None) == INVALID and "null" in _err(lib)
+
+
+def _append(lib, **kw):
+    a = dict(q=A, qs=16 * 128, k=A, v=A, ks=8 * 128, vs=8 * 128, slots=A, kc=A, vc=A, nb=64, bs=256,
+             bt=A, mb=16, ctx=A, b=0, maxc=4096, hq=16, hkv=8, d=128, ws=A, wsb=1 << 20, out=A,
+             os=16 * 128)
+    a.update(kw)
+    return lib.attn_decode_paged_append(a["q"], a["qs"], a["k"], a["v"], a["ks"], a["vs"], a["slots"],
+                                        a["kc"], a["vc"], a["nb"], a["bs"], a["bt"], a["mb"], a["ctx"],
+                                        a["b"], a["maxc"], a["hq"], a["hkv"], a["d"], 0.088, a["ws"],
+                                        a["wsb"], a["out"], a["os"], None)
+
+
+def test_decode_append_validation(lib):
+    assert _append(lib) == OK  # no sequences
+    assert _append(lib, hq=64, qs=64 * 128, os=64 * 128) == OK  # eight heads per kv head, d 128
+    assert _append(lib, b=-1) == INVALID and "bad sizes" in _err(lib)
+    assert _append(lib, hkv=3, hq=12) == UNSUPPORTED and "unsupported" in _err(lib)
+    assert _append(lib, ks=8 * 128 - 8) == INVALID and "stride" in _err(lib)
+    assert _append(lib, mb=1 << 20, bs=4096) == UNSUPPORTED and "capacity" in _err(lib)
+    assert _append(lib, nb=1 << 20, bs=4096, mb=16) == UNSUPPORTED and "2^31" in _err(lib)
+    assert _append(lib, b=4, slots=None) == INVALID and "null" in _err(lib)
+    assert _append(lib, b=4, k=MIS) == INVALID and "alignment" in _err(lib)
+    assert _append(lib, b=4, vs=8 * 128 + 4) == INVALID
