@@ -284,11 +284,18 @@ int attn_decode_paged_append(const kvp_bf16 *q, int64_t q_stride_tok, const kvp_
  * or other allocating routine.
  *
  * Arguments, results and errors are those of attn_decode_paged without
- * `workspace` / `workspace_bytes`.  In addition:
- * - a shape whose scratch need (attn_decode_workspace_size) exceeds 8 MiB is
- *   rejected with KVP_ERR_WORKSPACE and a message naming both sizes, before
- *   any other check; on a 152-SM GB300 every shape attn_decode_paged
- *   supports fits;
+ * `workspace` / `workspace_bytes`, and checked in the same order (messages
+ * name this entry point).  In addition:
+ * - after those checks, a call whose scratch need (what
+ *   attn_decode_workspace_size returns for it: CTAs x 2 x num_heads x
+ *   (head_dim + 4) x 4 bytes plus 4 bytes per CTA, with one CTA per 64
+ *   tokens of num_seqs x max_context_len, at most one per SM) exceeds 8 MiB
+ *   is rejected with KVP_ERR_WORKSPACE and a message naming both sizes.
+ *   Not every supported shape fits: on a 152-SM GB300, 64 query heads at
+ *   head_dim 128 (8 kv heads x 8) need up to 9.8 MiB and are rejected once
+ *   num_seqs x max_context_len exceeds 124 x 64 tokens; every other shape
+ *   attn_decode_paged supports (at most 32 query heads at head_dim 128, or
+ *   64 at head_dim 64) fits on GPUs of up to 240 SMs;
  * - every GPU that loads the library reserves the 8 MiB until the process
  *   exits;
  * - the first call on a device looks up the array's device address

@@ -260,9 +260,11 @@ def attn_decode_paged_append(q, k, v, slot_mapping, k_cache, v_cache, block_tabl
 
 
 def attn_decode_paged_noalloc(q, k_cache, v_cache, block_tables, context_lens, max_context_len: int,
-                              softmax_scale: float | None = None, out=None):
+                              out, softmax_scale: float | None = None):
     """attn_decode_paged without a workspace: the library's built-in scratch
-    is used (see include/kvpaged.h for who needs this and its limits)."""
+    is used (see include/kvpaged.h for who needs this and its limits).  The
+    caller passes ``out`` ([num_seqs, num_heads, head_dim] bf16): like the
+    entry point, this wrapper allocates no device memory."""
     import torch
     nb, bs, hkv, d = _cache_dims(k_cache, v_cache)
     dev = k_cache.device
@@ -275,9 +277,9 @@ def attn_decode_paged_noalloc(q, k_cache, v_cache, block_tables, context_lens, m
         raise ValueError("block_tables / context_lens must have one row per sequence")
     if not block_tables.is_contiguous() or not context_lens.is_contiguous():
         raise ValueError("block_tables / context_lens must be contiguous")
-    if out is None:
-        out = torch.empty((b, hq, d), dtype=torch.bfloat16, device=dev)
     _require(out, "out", torch.bfloat16, 3, dev)
+    if out.shape[0] != b:
+        raise ValueError("out must have one row per sequence")
     os_ = _rows(out, "out", hq, d)
     scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
     _check(library().attn_decode_paged_noalloc(

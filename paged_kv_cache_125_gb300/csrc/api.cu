@@ -3,6 +3,8 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
+#include <mutex>
 
 #include "kvp_internal.h"
 
@@ -27,27 +29,36 @@ int fail_cuda(cudaError_t e, const char* what) {
 __device__ int g_kvp_status;
 
 constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices];
+std::atomic<int*> g_status_ptr[kMaxDevices];
 int g_num_sms[kMaxDevices];
+std::mutex g_device_mu;
 
 // Per-device set-up: device address of the status word and the SM count.
+// Done once per device under a lock (first calls may come from several host
+// threads); later calls read the published pointer without locking.
 int device_info(int* dev_out, int** status, int* num_sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(KVP_ERR_UNSUPPORTED, "device %d", dev);
-  if (!g_status_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_kvp_status);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(status)");
-    int sms = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
-    g_num_sms[dev] = sms;
-    g_status_ptr[dev] = static_cast<int*>(p);
+  int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lock(g_device_mu);
+    p = g_status_ptr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+      void* addr = nullptr;
+      e = cudaGetSymbolAddress(&addr, g_kvp_status);
+      if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress(status)");
+      int sms = 0;
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
+      g_num_sms[dev] = sms;
+      p = static_cast<int*>(addr);
+      g_status_ptr[dev].store(p, std::memory_order_release);
+    }
   }
   *dev_out = dev;
-  *status = g_status_ptr[dev];
+  *status = p;
   *num_sms = g_num_sms[dev];
   return KVP_OK;
 }
@@ -70,6 +81,42 @@ int set_last_error(int code, const char* fmt, ...) {
   vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
   va_end(ap);
   return code;
+}
+
+// The argument checks of attn_decode_paged, in its order, with `fn` naming
+// the entry point in the message.  num_seqs == 0 passes before the pointer
+// checks (the call is then a no-op).
+int check_decode_args(const char* fn, const kvp_bf16* q, int64_t q_stride_tok,
+                      const kvp_bf16* k_cache, const kvp_bf16* v_cache, int64_t num_blocks,
+                      int block_size, const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, int num_seqs, int max_context_len,
+                      int num_heads, int num_kv_heads, int head_dim, const kvp_bf16* out,
+                      int64_t out_stride_tok) {
+  if (num_seqs < 0 || max_context_len < 0 || num_blocks <= 0 || block_size <= 0 ||
+      max_blocks_per_seq < 0)
+    return fail(KVP_ERR_INVALID_ARG, "%s: bad sizes", fn);
+  if (!decode_supported(num_heads, num_kv_heads, head_dim))
+    return fail(KVP_ERR_UNSUPPORTED, "%s: unsupported heads %d/%d or head_dim %d", fn, num_heads,
+                num_kv_heads, head_dim);
+  if (q_stride_tok < (int64_t)num_heads * head_dim || out_stride_tok < (int64_t)num_heads * head_dim)
+    return fail(KVP_ERR_INVALID_ARG, "%s: row stride too small", fn);
+  if ((int64_t)max_blocks_per_seq * block_size > (int64_t)1 << 30)
+    return fail(KVP_ERR_UNSUPPORTED, "%s: context capacity too large", fn);
+  if (num_seqs == 0) return KVP_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return fail(KVP_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      q_stride_tok % 8 || out_stride_tok % 8)
+    return fail(KVP_ERR_INVALID_ARG,
+                "%s: q, caches and out need 16-byte alignment and row strides that are multiples "
+                "of 8 elements",
+                fn);
+  return KVP_OK;
+}
+
+int device_sm_count(int* num_sms) {
+  int dev, *status;
+  return device_info(&dev, &status, num_sms);
 }
 
 }  // namespace kvp
@@ -168,27 +215,14 @@ int attn_decode_paged(const kvp_bf16* q, int64_t q_stride_tok, const kvp_bf16* k
                       int num_heads, int num_kv_heads, int head_dim, float softmax_scale,
                       void* workspace, size_t workspace_bytes, kvp_bf16* out,
                       int64_t out_stride_tok, kvp_stream_t stream) {
-  if (num_seqs < 0 || max_context_len < 0 || num_blocks <= 0 || block_size <= 0 ||
-      max_blocks_per_seq < 0)
-    return fail(KVP_ERR_INVALID_ARG, "attn_decode_paged: bad sizes");
-  if (!kvp::decode_supported(num_heads, num_kv_heads, head_dim))
-    return fail(KVP_ERR_UNSUPPORTED,
-                "attn_decode_paged: unsupported heads %d/%d or head_dim %d", num_heads,
-                num_kv_heads, head_dim);
-  if (q_stride_tok < (int64_t)num_heads * head_dim || out_stride_tok < (int64_t)num_heads * head_dim)
-    return fail(KVP_ERR_INVALID_ARG, "attn_decode_paged: row stride too small");
-  if ((int64_t)max_blocks_per_seq * block_size > (int64_t)1 << 30)
-    return fail(KVP_ERR_UNSUPPORTED, "attn_decode_paged: context capacity too large");
+  int rc = kvp::check_decode_args("attn_decode_paged", q, q_stride_tok, k_cache, v_cache,
+                                  num_blocks, block_size, block_tables, max_blocks_per_seq,
+                                  context_lens, num_seqs, max_context_len, num_heads, num_kv_heads,
+                                  head_dim, out, out_stride_tok);
+  if (rc) return rc;
   if (num_seqs == 0) return KVP_OK;
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-    return fail(KVP_ERR_INVALID_ARG, "attn_decode_paged: null pointer");
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
-      q_stride_tok % 8 || out_stride_tok % 8)
-    return fail(KVP_ERR_INVALID_ARG,
-                "attn_decode_paged: q, caches and out need 16-byte alignment and row strides "
-                "that are multiples of 8 elements");
   int dev, *status, sms;
-  int rc = device_info(&dev, &status, &sms);
+  rc = device_info(&dev, &status, &sms);
   if (rc) return rc;
   const kvp::DecodePlan plan = kvp::plan_decode(num_seqs, num_heads, head_dim, max_context_len, sms);
   if (!workspace || workspace_bytes < plan.total_bytes || !aligned16(workspace))

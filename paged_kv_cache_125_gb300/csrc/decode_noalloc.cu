@@ -52,19 +52,27 @@ extern "C" int attn_decode_paged_noalloc(const kvp_bf16* q, int64_t q_stride_tok
                                          int max_context_len, int num_heads, int num_kv_heads,
                                          int head_dim, float softmax_scale, kvp_bf16* out,
                                          int64_t out_stride_tok, kvp_stream_t stream) {
-  if (num_seqs > 0) {
-    const size_t need =
-        attn_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len, block_size);
-    if (need == 0) return KVP_ERR_INVALID_ARG;  // message already set
-    if (need > kNoAllocScratchBytes)
-      return kvp::set_last_error(
-          KVP_ERR_WORKSPACE,
-          "attn_decode_paged_noalloc: this shape needs %zu bytes of scratch, more than the %zu "
-          "bytes the built-in scratch holds; use attn_decode_paged with a caller workspace",
-          need, kNoAllocScratchBytes);
-  }
+  // attn_decode_paged's own checks first, so a bad argument is reported as it
+  // would be there; the scratch size after them.
+  int rc = kvp::check_decode_args("attn_decode_paged_noalloc", q, q_stride_tok, k_cache, v_cache,
+                                  num_blocks, block_size, block_tables, max_blocks_per_seq,
+                                  context_lens, num_seqs, max_context_len, num_heads, num_kv_heads,
+                                  head_dim, out, out_stride_tok);
+  if (rc != KVP_OK) return rc;
+  if (num_seqs == 0) return KVP_OK;
+  int sms = 0;
+  rc = kvp::device_sm_count(&sms);
+  if (rc != KVP_OK) return rc;
+  const size_t need =
+      kvp::plan_decode(num_seqs, num_heads, head_dim, max_context_len, sms).total_bytes;
+  if (need > kNoAllocScratchBytes)
+    return kvp::set_last_error(
+        KVP_ERR_WORKSPACE,
+        "attn_decode_paged_noalloc: this shape needs %zu bytes of scratch, more than the %zu "
+        "bytes the built-in scratch holds; use attn_decode_paged with a caller workspace",
+        need, kNoAllocScratchBytes);
   void* scratch = nullptr;
-  const int rc = scratch_address(&scratch);
+  rc = scratch_address(&scratch);
   if (rc != KVP_OK) return rc;
   // The split kernel writes every partial and boundary record the merge reads
   // within the same call, so nothing in the scratch has to start at zero.

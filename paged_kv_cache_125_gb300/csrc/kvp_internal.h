@@ -12,6 +12,15 @@ namespace kvp {
 
 // api.cu: records the calling thread's message for kvp_last_error(); returns code.
 int set_last_error(int code, const char* fmt, ...);
+// api.cu: attn_decode_paged's argument checks (message names `fn`); the
+// current device's SM count (set-up on first use per device).
+int check_decode_args(const char* fn, const kvp_bf16* q, int64_t q_stride_tok,
+                      const kvp_bf16* k_cache, const kvp_bf16* v_cache, int64_t num_blocks,
+                      int block_size, const int32_t* block_tables, int max_blocks_per_seq,
+                      const int32_t* context_lens, int num_seqs, int max_context_len,
+                      int num_heads, int num_kv_heads, int head_dim, const kvp_bf16* out,
+                      int64_t out_stride_tok);
+int device_sm_count(int* num_sms);
 
 // selftest.cu: one thread waits on a barrier (arrive: after arriving on it
 // itself; else nothing arrives and the 2 ms wait expires).

@@ -41,7 +41,7 @@ def test_decode_refuses_host_tensors():
                                      torch.zeros((2, 2, 64), dtype=bf16), torch.zeros(2, dtype=i32),
                                      kc, vc, bt, ctx, 48)
     with pytest.raises(ValueError, match="CUDA"):
-        kvp.attn_decode_paged_noalloc(q, kc, vc, bt, ctx, 48)
+        kvp.attn_decode_paged_noalloc(q, kc, vc, bt, ctx, 48, out=torch.zeros_like(q))
 
 
 def test_prefill_refuses_host_tensors():
