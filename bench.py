@@ -816,23 +816,18 @@ def measure_scheduler():
     schedule + metadata + postprocess per step, native C++ scheduler (through
     its C ABI) against the Python replica of the same policy."""
     from paged_kv_cache_125_gb300 import engine_trace as E
-    from paged_kv_cache_125_gb300 import workloads as W
     from paged_kv_cache_125_gb300.scheduler import NativeScheduler
     reqs = E.make_requests(256, (100, 1024), (100, 1024))
 
     def py_loop():
         sch = E.Scheduler(512, 16384, 768, 256)
         for i, (t, o) in enumerate(reqs):
-            sch.add(E.Sequence(i, t, o, 256))
+            sch.submit(E.Request(i, t, o, 256))
         n = 0
-        while not sch.is_finished():
-            seqs, pre = sch.schedule()
-            lens, tabs = [len(x) for x in seqs], [list(x.block_table) for x in seqs]
-            if pre:
-                W.prefill_metadata(lens, [x.num_cached_tokens for x in seqs], tabs, 256)
-            else:
-                W.decode_metadata(lens, tabs, 256)
-            sch.postprocess(seqs, [E.synthetic_token(x.seq_id, len(x)) for x in seqs])
+        while not sch.done():
+            seqs, pre = sch.next_batch()
+            E.step_metadata(seqs, pre, 256)
+            sch.commit(seqs, [E.synthetic_token(x.rid, len(x)) for x in seqs])
             n += 1
         return n
 

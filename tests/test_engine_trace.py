@@ -8,30 +8,30 @@ from paged_kv_cache_125_gb300 import workloads as W
 
 
 def _check_step(st, sched, bs):
-    bm = sched.block_manager
-    nb = len(bm.blocks)
-    free, used = set(bm.free_block_ids), bm.used_block_ids
+    pool = sched.pool
+    nb = pool.num_blocks
+    free, used = set(pool.free_queue), pool.in_use()
     assert not (free & used) and len(free) + len(used) == nb, "free and used must partition the pool"
-    assert len(bm.free_block_ids) == len(free), "free list holds no duplicates"
+    assert pool.num_free == len(free), "free queue holds no duplicates"
     # reference counts equal the number of tables holding each block
     holders = {}
     for seq in sched.running:
-        for b in seq.block_table:
+        for b in seq.table:
             holders[b] = holders.get(b, 0) + 1
     for b in range(nb):
-        assert bm.blocks[b].ref_count == holders.get(b, 0)
+        assert pool.refs[b] == holders.get(b, 0)
     m = st.meta
     slots = m.slot_mapping.tolist()
     assert len(set(slots)) == len(slots), "a slot is written twice in one step"
-    seqs = {s.seq_id: s for s in sched.running}
+    seqs = {s.rid: s for s in sched.running}
     if st.is_prefill:
         cq, ck = m.cu_seqlens_q.tolist(), m.cu_seqlens_k.tolist()
         at = 0
         for i, sid in enumerate(st.seq_ids):
             s = seqs[sid]
             assert ck[i + 1] - ck[i] == len(s)
-            assert ck[i + 1] - ck[i] - (cq[i + 1] - cq[i]) == s.num_cached_tokens
-            want = W.slots_of_positions(s.block_table, range(s.num_cached_tokens, len(s)), bs)
+            assert ck[i + 1] - ck[i] - (cq[i + 1] - cq[i]) == s.cached
+            want = W.slots_of_positions(s.table, range(s.cached, len(s)), bs)
             assert slots[at:at + len(want)] == want
             at += len(want)
         assert at == len(slots)
@@ -40,8 +40,8 @@ def _check_step(st, sched, bs):
         for i, sid in enumerate(st.seq_ids):
             s = seqs[sid]
             assert m.context_lens[i] == len(s)
-            assert slots[i] == W.slots_of_positions(s.block_table, [len(s) - 1], bs)[0]
-            assert len(s.block_table) == s.num_blocks
+            assert slots[i] == W.slots_of_positions(s.table, [len(s) - 1], bs)[0]
+            assert len(s.table) == s.blocks_needed
 
 
 def test_small_trace_invariants_and_completion():
@@ -54,9 +54,9 @@ def test_small_trace_invariants_and_completion():
         _check_step(st, sched, bs)
         steps += 1
         prefills += st.is_prefill
-    assert sched.is_finished() and steps > 50 and prefills >= 2
-    assert sched.num_preemptions > 0, "the small pool must force preemption"
-    assert len(sched.block_manager.free_block_ids) == 40
+    assert sched.done() and steps > 50 and prefills >= 2
+    assert sched.preemptions > 0, "the small pool must force preemption"
+    assert sched.pool.num_free == 40
 
 
 def test_every_request_gets_exactly_max_tokens():
@@ -68,8 +68,8 @@ def test_every_request_gets_exactly_max_tokens():
                                     num_blocks=12, block_size=16, prompt_range=(5, 40),
                                     output_range=(3, 30)):
         for sid in st.seq_ids:
-            s = next(x for x in list(sched.running) if x.seq_id == sid)
-            counts[sid] = s.num_completion_tokens + 1
+            s = next(x for x in list(sched.running) if x.rid == sid)
+            counts[sid] = s.generated + 1
     for i, (toks, out_len) in enumerate(reqs):
         assert counts[i] == out_len
 
@@ -83,11 +83,11 @@ def test_prefix_cache_hits_after_preemption_are_consistent():
                                     output_range=(10, 60)):
         if st.is_prefill:
             for sid in st.seq_ids:
-                s = next(x for x in sched.running if x.seq_id == sid)
-                assert s.num_cached_tokens % 16 == 0
-                for i in range(s.num_cached_blocks):
-                    assert sched.block_manager.blocks[s.block_table[i]].token_ids == s.block(i)
-                hits += s.num_cached_blocks
+                s = next(x for x in sched.running if x.rid == sid)
+                assert s.cached % 16 == 0
+                for i in range(s.cached_blocks):
+                    assert sched.pool.content[s.table[i]] == s.block_tokens(i)
+                hits += s.cached_blocks
     assert hits > 0
 
 
@@ -95,7 +95,7 @@ def test_chained_hash_distinguishes_prefixes():
     """Pages' example: [A, B, C] and [A, B, D] share the hashes of their first
     two blocks and differ on the third."""
     A, B, C, D = [1] * 4, [2] * 4, [3] * 4, [4] * 4
-    h = E.BlockManager.compute_hash
+    h = E.chain_hash
     ha = h(A)
     hb = h(B, ha)
     assert h(B, h(A)) == hb and h(C, hb) != h(D, hb) and h(B) != hb
@@ -110,4 +110,4 @@ def test_full_trace_config5_invariants():
         if n % 25 == 0:
             _check_step(st, sched, 256)
         n += 1
-    assert sched.is_finished() and sched.num_preemptions > 0
+    assert sched.done() and sched.preemptions > 0

@@ -28,34 +28,34 @@ def _replay(requests, num_blocks, block_size, max_num_seqs, max_batched, max_ste
     py = E.Scheduler(max_num_seqs, max_batched, num_blocks, block_size)
     nat = NativeScheduler(num_blocks, block_size, max_num_seqs, max_batched)
     for i, (toks, out_len) in enumerate(requests):
-        py.add(E.Sequence(i, toks, out_len, block_size))
+        py.submit(E.Request(i, toks, out_len, block_size))
         nat.add(i, toks, out_len)
     steps = prefills = 0
-    while not py.is_finished():
+    while not py.done():
         assert not nat.is_finished()
-        seqs, is_prefill = py.schedule()
+        seqs, is_prefill = py.next_batch()
         ids, nat_prefill, meta = nat.step()
-        assert ids == [s.seq_id for s in seqs] and nat_prefill == is_prefill, steps
+        assert ids == [s.rid for s in seqs] and nat_prefill == is_prefill, steps
         if is_prefill:
-            ref = W.prefill_metadata([len(s) for s in seqs], [s.num_cached_tokens for s in seqs],
-                                     [list(s.block_table) for s in seqs], block_size)
+            ref = W.prefill_metadata([len(s) for s in seqs], [s.cached for s in seqs],
+                                     [list(s.table) for s in seqs], block_size)
             prefills += 1
         else:
-            ref = W.decode_metadata([len(s) for s in seqs], [list(s.block_table) for s in seqs],
+            ref = W.decode_metadata([len(s) for s in seqs], [list(s.table) for s in seqs],
                                     block_size)
         _same_meta(meta, ref, is_prefill)
         for s in seqs:
-            st = nat.seq_state(s.seq_id)
-            assert st["num_cached_tokens"] == s.num_cached_tokens and st["block_table"] == s.block_table
-        assert nat.num_preemptions == py.num_preemptions
-        assert nat.num_free_blocks == len(py.block_manager.free_block_ids)
-        toks = [E.synthetic_token(s.seq_id, len(s)) for s in seqs]
-        py.postprocess(seqs, toks)
+            st = nat.seq_state(s.rid)
+            assert st["num_cached_tokens"] == s.cached and st["block_table"] == s.table
+        assert nat.num_preemptions == py.preemptions
+        assert nat.num_free_blocks == py.pool.num_free
+        toks = [E.synthetic_token(s.rid, len(s)) for s in seqs]
+        py.commit(seqs, toks)
         nat.postprocess(toks)
         steps += 1
         assert steps < max_steps
     assert nat.is_finished()
-    return steps, prefills, py.num_preemptions
+    return steps, prefills, py.preemptions
 
 
 def test_small_pool_with_preemption_matches_python_replica():
