@@ -59,6 +59,8 @@ TRAFFIC = {
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
                 "sha256": "7202843ebee04788acca15514bba8b861c474cba85d4a42595a64edce6a83eb4",
                 "bytes": 124059136 + 34817536},
+    # the prefill workload's suffix store (7.2k rows), one ncu capture
+    "kv_store": {"file": "paged_kv_cache_125_gb300/csrc/kv_store.cu", "sha256": None, "bytes": None},
 }
 
 
@@ -75,8 +77,12 @@ def parse_args():
     p.add_argument("--no-copy-blocks", action="store_true")
     p.add_argument("--no-large", action="store_true", help="skip the 150 GB decode B512 line")
     p.add_argument("--no-trace", action="store_true", help="skip the engine-trace replay line")
-    p.add_argument("--only", choices=["decode", "prefill"], default=None,
-                   help="run one half only (profiling); the JSON line then carries that half")
+    p.add_argument("--only", choices=["decode", "prefill", "decode_b512"], default=None,
+                   help="run one part only (profiling); the JSON line then carries that part")
+    p.add_argument("--b512-batch", type=int, default=512,
+                   help="sequences of the decode B512 line (a smaller batch profiles the same kernel)")
+    p.add_argument("--b512-blocks", type=int, default=None,
+                   help="pool blocks of the decode B512 line (default: the 150 GB pool)")
     p.add_argument("--sets", type=int, default=N_SETS, help="input sets in rotation")
     return p.parse_args()
 
@@ -238,6 +244,16 @@ def append_call(kvp, s, w, ws):
                                  softmax_scale=w.scale, workspace=ws, out=s.out)
 
 
+def prefill_append_call(kvp, s, w):
+    """The prefill step in one call: the store of the new rows fused into the prefill."""
+    kvp.attn_prefill_varlen_append(s.q, s.k, s.v, s.slots, s.cu_q, s.cu_k, s.max_q, s.max_k, s.kc, s.vc,
+                                   block_tables=s.bt, softmax_scale=w.scale, out=s.out)
+
+
+def no_call(s):
+    pass
+
+
 def prefill_call(kvp, s, w):
     kvp.attn_prefill_varlen(s.q, s.cu_q, s.cu_k, s.max_q, s.max_k, k=s.k, v=s.v, k_cache=s.kc,
                             v_cache=s.vc, block_tables=s.bt, num_kv_heads=w.num_kv_heads,
@@ -354,8 +370,7 @@ def timed_loop_eager(store_fn, attn_fn, sets, steps, warmup, world):
     for i in range(warmup):
         store_fn(sets[i % n])
         attn_fn(sets[i % n])
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -363,16 +378,18 @@ def timed_loop_eager(store_fn, attn_fn, sets, steps, warmup, world):
     w0 = time.perf_counter()
     start.record()
     for i in range(steps):
-        store_fn(sets[i % n])
         evs[i][0].record()
-        attn_fn(sets[i % n])
+        store_fn(sets[i % n])
         evs[i][1].record()
+        attn_fn(sets[i % n])
+        evs[i][2].record()
     stop.record()
     torch.cuda.synchronize()
     w1 = time.perf_counter()
     barrier(world)
     ms_step = start.elapsed_time(stop) / steps
-    durs = [a.elapsed_time(b) for a, b in evs]
+    durs = [b.elapsed_time(c) for a, b, c in evs]
+    timed_loop_eager.last_store_ms = statistics.mean(a.elapsed_time(b) for a, b, c in evs)
     return ms_step, statistics.mean(durs), (w0, w1)
 
 
@@ -538,47 +555,84 @@ def measure_decode(args, kvp, W, dev, stream, world, peaks):
 
 
 def measure_prefill(args, kvp, W, dev, stream, world, peaks):
+    """The prefill configuration (8 prompts U[256, 2048], 0-2 cached blocks,
+    32/8/128, bs 256).  A step is attn_prefill_varlen_append: the store of
+    the uncached suffix fused into the paged prefill, launched eagerly as the
+    engine runs prefill steps.  The same step as two launches (kv_store, then
+    attn_prefill_varlen) is timed in a second loop, with the store's own
+    roofline."""
     wp = W.config3_prefill()
     flops = prefill_flops(wp)
     psets = [DeviceSet(wp, dev) for _ in range(args.sets)]
     psteps = args.prefill_steps or max(50, args.steps // 4)
-    ms_pstep, ms_prefill, pwin = timed_loop_eager(lambda s_: store_call(kvp, s_),
-                                                  lambda s_: prefill_call(kvp, s_, wp), psets, psteps,
-                                                  args.warmup, world)
+    ms_pstep, ms_fused, pwin = timed_loop_eager(no_call, lambda s_: prefill_append_call(kvp, s_, wp),
+                                                psets, psteps, args.warmup, world)
     assert kvp.device_status() == 0, "device status after the timed prefill loop"
+    ms_step2, ms_prefill, pwin2 = timed_loop_eager(lambda s_: store_call(kvp, s_),
+                                                   lambda s_: prefill_call(kvp, s_, wp), psets, psteps,
+                                                   args.warmup, world)
+    ms_store = timed_loop_eager.last_store_ms
+    assert kvp.device_status() == 0, "device status after the two-call prefill loop"
     flops_per_s, ms_pstep = aggregate(flops, ms_pstep, world)
-    tflops_kernel = flops / (ms_prefill * 1e-3) / 1e12
+    flops_per_s2, ms_step2 = aggregate(flops, ms_step2, world)
+    tf_fused = flops / (ms_fused * 1e-3) / 1e12
+    tf_prefill = flops / (ms_prefill * 1e-3) / 1e12
+    # the suffix store: every new row's K and V read and written, plus slot_mapping
+    n_new = int(wp.steps[0].store.slot_mapping.shape[0])
+    store_bytes = n_new * (4 * wp.num_kv_heads * wp.head_dim * 2 + 4)
+    store_gbs = store_bytes / (ms_store * 1e-3) / 1e9
     del psets
-    return {"window": pwin,
+    return {"window": pwin, "window2": pwin2,
             "line": {"workload": wp.description, "value": round(flops_per_s / 1e12, 2),
                      "unit": "TFLOP/s", "ms_per_step": round(ms_pstep, 4), "steps": psteps,
-                     "step": "kv_store of the uncached suffix + attn_prefill_varlen (paged, prefix cache), "
-                             "launched eagerly as the engine runs prefill steps",
-                     "roofline": {"kernel": "attn_prefill_varlen", "bound": "tensor",
-                                  "achieved": round(tflops_kernel, 1), "peak": peaks["bf16_tflops"],
-                                  "unit": "TFLOP/s", "frac": round(tflops_kernel / peaks["bf16_tflops"], 4),
+                     "step": "attn_prefill_varlen_append: kv_store of the uncached suffix fused into the "
+                             "paged prefill, launched eagerly as the engine runs prefill steps",
+                     "frac_of_bf16_burst": round(flops_per_s / 1e12 / peaks["bf16_tflops"], 4),
+                     "roofline": {"kernel": "attn_prefill_varlen_append (store + prefill)", "bound": "tensor",
+                                  "achieved": round(tf_fused, 1), "peak": peaks["bf16_tflops"],
+                                  "unit": "TFLOP/s", "frac": round(tf_fused / peaks["bf16_tflops"], 4),
                                   "traffic": traffic_for("prefill"), "algorithmic_flops": flops,
                                   "peak_source": peaks["source"] + " bf16 burst",
-                                  "ms_per_launch": round(ms_prefill, 5)}}}
+                                  "ms_per_launch": round(ms_fused, 5)},
+                     "two_calls": {
+                         "step": "kv_store of the uncached suffix, then attn_prefill_varlen (two launches)",
+                         "value": round(flops_per_s2 / 1e12, 2), "unit": "TFLOP/s",
+                         "ms_per_step": round(ms_step2, 4),
+                         "roofline": {"kernel": "attn_prefill_varlen", "bound": "tensor",
+                                      "achieved": round(tf_prefill, 1), "peak": peaks["bf16_tflops"],
+                                      "unit": "TFLOP/s", "frac": round(tf_prefill / peaks["bf16_tflops"], 4),
+                                      "algorithmic_flops": flops, "peak_source": peaks["source"] + " bf16 burst",
+                                      "ms_per_launch": round(ms_prefill, 5)},
+                         "store": {"workload": f"kv_store of the prefill step's {n_new} new rows "
+                                               f"({wp.num_kv_heads}x{wp.head_dim} bf16 K and V each)",
+                                   "ms_per_launch": round(ms_store, 5),
+                                   "roofline": {"kernel": "kv_store", "bound": "hbm",
+                                                "achieved": round(store_gbs, 1), "peak": peaks["hbm_gbs"],
+                                                "unit": "GB/s",
+                                                "frac": round(store_gbs / peaks["hbm_gbs"], 4),
+                                                "traffic": traffic_for("kv_store"),
+                                                "algorithmic_bytes": store_bytes,
+                                                "peak_source": peaks["source"]}}}}}
 
 
 def measure_mixed(args, kvp, W, dev, stream, world, peaks):
     """One engine step mixing chunked prefill and decode in a single varlen
     paged prefill call (4 prompt chunks, 3772 tokens, + 128 decode rows,
-    32/8/128): store of the new rows + the attention call, launched eagerly
-    over 2 input sets in rotation."""
+    32/8/128): attn_prefill_varlen_append (the store of the new rows fused
+    into the attention call), launched eagerly over 2 input sets in rotation."""
     wm = W.mixed_step_workload()
     flops = prefill_flops(wm)
     m = wm.steps[0].attn.meta
-    # algorithmic bytes: K and V of every sequence's keys once per kv head, q read, out written
+    # algorithmic bytes: K and V of every sequence's keys once per kv head, q read, out written,
+    # the new rows read and stored
     kv_bytes = int(m.cu_seqlens_k[-1]) * wm.num_kv_heads * wm.head_dim * 2 * 2
     qo_bytes = int(m.cu_seqlens_q[-1]) * wm.num_heads * wm.head_dim * 2 * 2
-    nbytes = kv_bytes + qo_bytes
+    st_bytes = int(m.cu_seqlens_q[-1]) * (4 * wm.num_kv_heads * wm.head_dim * 2 + 4)
+    nbytes = kv_bytes + qo_bytes + st_bytes
     msets = [DeviceSet(wm, dev) for _ in range(2)]
     steps = max(50, min(400, args.steps // 10))
-    ms_step, ms_call, win = timed_loop_eager(lambda s_: store_call(kvp, s_),
-                                             lambda s_: prefill_call(kvp, s_, wm), msets, steps,
-                                             args.warmup, world)
+    ms_step, ms_call, win = timed_loop_eager(no_call, lambda s_: prefill_append_call(kvp, s_, wm), msets,
+                                             steps, args.warmup, world)
     assert kvp.device_status() == 0, "device status after the mixed loop"
     fps, ms_step = aggregate(flops, ms_step, world)
     tf_call = flops / (ms_call * 1e-3) / 1e12
@@ -589,8 +643,8 @@ def measure_mixed(args, kvp, W, dev, stream, world, peaks):
     return {"window": win, "steps": steps,
             "line": {"workload": wm.description, "value": round(fps / 1e12, 2), "unit": "TFLOP/s",
                      "ms_per_step": round(ms_step, 4), "steps": steps,
-                     "step": "kv_store of all new rows + attn_prefill_varlen over chunks and decode rows",
-                     "roofline": ({"kernel": "attn_prefill_varlen (mixed)", "bound": "hbm",
+                     "step": "attn_prefill_varlen_append over chunks and decode rows (store fused)",
+                     "roofline": ({"kernel": "attn_prefill_varlen_append (mixed)", "bound": "hbm",
                                    "achieved": round(gbs_call, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                    "frac": round(gbs_call / peaks["hbm_gbs"], 4), "traffic": None,
                                    "algorithmic_bytes": nbytes, "peak_source": peaks["source"],
@@ -599,7 +653,7 @@ def measure_mixed(args, kvp, W, dev, stream, world, peaks):
                                               "frac_of_bf16_burst": round(tf_call / peaks["bf16_tflops"], 4),
                                               "algorithmic_flops": flops}}
                                   if hbm_bound else
-                                  {"kernel": "attn_prefill_varlen (mixed)", "bound": "tensor",
+                                  {"kernel": "attn_prefill_varlen_append (mixed)", "bound": "tensor",
                                    "achieved": round(tf_call, 1), "peak": peaks["bf16_tflops"],
                                    "unit": "TFLOP/s", "frac": round(tf_call / peaks["bf16_tflops"], 4),
                                    "traffic": None, "algorithmic_flops": flops,
@@ -685,14 +739,17 @@ def measure_decode_large(args, kvp, W, dev, stream, world, peaks):
     import torch
     torch.cuda.empty_cache()
     free, _ = torch.cuda.mem_get_info(dev)
-    if free < 165e9:
+    blocks = args.b512_blocks or W.CONFIG4_POOL_BLOCKS
+    need = blocks * 2 * 256 * 8 * 128 * 2 * 1.1
+    if free < need:
         return {"window": None, "steps": 0,
-                "line": {"skipped": f"needs ~160 GB free device memory, {free / 1e9:.0f} GB free"}}
-    w = W.config4_decode(device=dev)
+                "line": {"skipped": f"needs ~{need / 1e9:.0f} GB free device memory, "
+                                    f"{free / 1e9:.0f} GB free"}}
+    w = W.config4_decode(num_blocks=blocks, batch=args.b512_batch, device=dev)
     store_b, dec_b = decode_bytes(w)
     ds = DeviceSet(w, dev)
     m = w.steps[0].attn.meta
-    ws = torch.empty(kvp.attn_decode_workspace_size(512, 32, 128, m.max_context_len, 256),
+    ws = torch.empty(kvp.attn_decode_workspace_size(args.b512_batch, 32, 128, m.max_context_len, 256),
                      dtype=torch.uint8, device=dev)
     ag = capture(lambda s_: append_call(kvp, s_, w, ws), [ds], stream)
     steps = max(10, min(100, args.steps // 100))
@@ -714,83 +771,108 @@ def measure_decode_large(args, kvp, W, dev, stream, world, peaks):
                                   "ms_per_launch": round(ms_dec, 5)}}}
 
 
+def measure_decode_group8(args, kvp, W, dev, stream, world, peaks):
+    """Decode with eight query heads per kv head at head_dim 128 (64/8/128):
+    the decode B64 batch (64 sequences, ctx U[512, 4096], bs 256, 2048-block
+    pool) with that attention shape, store fused, 2 input sets in rotation
+    (2.3 GB of pools)."""
+    import torch
+    ctx = torch.randint(512, 4097, (64,), generator=W.generator(W.SEED_LENGTHS)).tolist()
+    w = W.decode_workload("decode_b64_g8", ctx, 64, 8, 128, 256, 2048,
+                          description="decode: B64 64/8/128 bs256 NB2048 ctx U[512,4096]")
+    store_b, dec_b = decode_bytes(w)
+    sets = [DeviceSet(w, dev) for _ in range(2)]
+    ws = torch.empty(kvp.attn_decode_workspace_size(64, 64, 128, w.steps[0].attn.meta.max_context_len, 256),
+                     dtype=torch.uint8, device=dev)
+    graphs = capture(lambda s_: append_call(kvp, s_, w, ws), sets, stream)
+    steps = max(20, min(200, args.steps // 25))
+    ms_step, ms_call, win = timed_loop_single(graphs, steps, max(3, args.warmup // 4), world)
+    assert kvp.device_status() == 0, "device status after the group-8 decode loop"
+    achieved = (store_b + dec_b) / (ms_call * 1e-3) / 1e9
+    del graphs, sets, ws
+    torch.cuda.empty_cache()
+    return {"window": win, "steps": steps,
+            "line": {"workload": w.description, "ms_per_step": round(ms_step, 4), "steps": steps,
+                     "step": "attn_decode_paged_append (store fused)",
+                     "roofline": {"kernel": "attn_decode_paged_append (store + split + merge)",
+                                  "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                                  "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                                  "traffic": None, "algorithmic_bytes": store_b + dec_b,
+                                  "peak_source": peaks["source"], "ms_per_launch": round(ms_call, 5)}}}
+
+
 def measure_trace(args, kvp, dev, stream, world, peaks):
     """Engine-trace replay: 256 requests (prompts and outputs U[100, 1024]),
     scheduled by the native scheduler (prefill first, max 512 seqs / 16384
     tokens per step, 768 blocks of 256 tokens), every step running kv_store +
     prefill or decode attention on all 28 layers of a Qwen3-0.6B attention
-    shape (16/8/128).  Prefill steps are launched eagerly; decode steps replay
-    one 28-layer graph per batch-size bucket (LayeredDecodeGraphs), as the
-    pages' engine does.  Aggregate GB/s over the decode steps (algorithmic
-    bytes) and TFLOP/s over the prefill steps (causal FLOPs), each timed by an
-    event pair around the step's 28 layers (for decode: the copy of the
-    step's packed metadata into the graph's buffer and the replay)."""
+    shape (16/8/128), with per-layer q/k/v drawn on the device.  The step loop
+    is ``EngineReplay`` (the one the GPU trace test checks against the
+    oracle): prefill steps are launched eagerly; decode steps replay one
+    28-layer graph per batch-size bucket, as the pages' engine does.
+    Aggregate GB/s over the decode steps (algorithmic bytes) and TFLOP/s over
+    the prefill steps (causal FLOPs), each timed by an event pair around
+    ``launch`` (for decode: the copy of the step's packed metadata into the
+    graph's buffer and the replay).  Prefill steps are also broken down by
+    their query tokens."""
     import torch
     from paged_kv_cache_125_gb300 import engine_trace as E
-    from paged_kv_cache_125_gb300.graphs import LayeredDecodeGraphs
-    from paged_kv_cache_125_gb300.scheduler import NativeScheduler
+    from paged_kv_cache_125_gb300.engine_replay import EngineReplay, decode_bytes, prefill_flops
     layers, hq, hkv, d, bs, nb = 28, 16, 8, 128, 256, 768
-    scale = d ** -0.5
     torch.cuda.empty_cache()
-    kv = torch.full((2, layers, nb, bs, hkv, d), float("nan"), dtype=torch.bfloat16, device=dev)
-    sch = NativeScheduler(nb, bs, 512, 16384)
     reqs = E.make_requests(256, (100, 1024), (100, 1024))
-    for i, (t, o) in enumerate(reqs):
-        sch.add(i, t, o)
-    max_blocks = max((len(t) + o + bs - 1) // bs for t, o in reqs)
-    graphs = LayeredDecodeGraphs([(kv[0, l_], kv[1, l_]) for l_ in range(layers)], hq, max_blocks,
-                                 max_bs=512, softmax_scale=scale, stream=stream)
+    eng = EngineReplay(reqs, layers, hq, hkv, d, bs, nb, 512, 16384, dev, stream=stream)
     gq = torch.Generator(device=dev).manual_seed(5)
-    meta_len = graphs.meta.numel()
-    row = hkv * d * 2
     recs = []
     w0 = time.perf_counter()
-    while not sch.is_finished():
-        ids, pre, m = sch.step()
-        n = int(m.cu_seqlens_q[-1]) if pre else len(ids)
-        if pre:
-            q = torch.randn((n, hq, d), generator=gq, device=dev).to(torch.bfloat16)
-            k = torch.randn((n, hkv, d), generator=gq, device=dev).to(torch.bfloat16)
-            v = torch.randn((n, hkv, d), generator=gq, device=dev).to(torch.bfloat16)
+    while not eng.done():
+        st = eng.schedule()
+        n = st.num_new
+        if st.is_prefill:
+            q = torch.randn((layers, n, hq, d), generator=gq, device=dev).to(torch.bfloat16)
+            k = torch.randn((layers, n, hkv, d), generator=gq, device=dev).to(torch.bfloat16)
+            v = torch.randn((layers, n, hkv, d), generator=gq, device=dev).to(torch.bfloat16)
+            work = prefill_flops(st.meta, d, hq)
         else:  # every layer's new rows, straight into the graph's buffers
-            graphs.q[:, :n].copy_(torch.randn((layers, n, hq, d), generator=gq, device=dev))
-            graphs.k[:, :n].copy_(torch.randn((layers, n, hkv, d), generator=gq, device=dev))
-            graphs.v[:, :n].copy_(torch.randn((layers, n, hkv, d), generator=gq, device=dev))
-        if pre:
-            slots = m.slot_mapping.to(dev, non_blocking=True)
-            cq, ck = m.cu_seqlens_q.to(dev, non_blocking=True), m.cu_seqlens_k.to(dev, non_blocking=True)
-            bt = None if m.block_tables is None else m.block_tables.to(dev, non_blocking=True)
-            ql = (m.cu_seqlens_q[1:] - m.cu_seqlens_q[:-1]).long()
-            kl = (m.cu_seqlens_k[1:] - m.cu_seqlens_k[:-1]).long()
-            work = 4 * d * hq * int((ql * (kl - ql) + ql * (ql + 1) // 2).sum())
-        else:  # the step's metadata, packed for its bucket in pinned memory: one copy
-            packed = graphs.pack(n, m.slot_mapping, m.block_tables, m.context_lens,
-                                 out=torch.empty((meta_len,), dtype=torch.int32, pin_memory=True))
-            c = m.context_lens.long()
-            work = 4 * n * row + int(c.sum()) * row * 2 + 2 * n * hq * d * 2 + \
-                int(((c + bs - 1) // bs).sum()) * 4 + n * 4
+            q, k, v = eng.decode_inputs(st)
+            q.copy_(torch.randn(q.shape, generator=gq, device=dev))
+            k.copy_(torch.randn(k.shape, generator=gq, device=dev))
+            v.copy_(torch.randn(v.shape, generator=gq, device=dev))
+            work = decode_bytes(st.meta, n, hq, hkv, d, bs)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        if pre:
-            for layer in range(layers):
-                kc, vc = kv[0, layer], kv[1, layer]
-                kvp.kv_store(k, v, slots, kc, vc)
-                kvp.attn_prefill_varlen(q, cq, ck, m.max_seqlen_q, m.max_seqlen_k, k=k, v=v, k_cache=kc,
-                                        v_cache=vc, block_tables=bt, num_kv_heads=hkv, softmax_scale=scale)
-        else:
-            graphs.run_packed(n, packed)
+        eng.launch(st, q, k, v)
         b.record()
-        recs.append((pre, work * layers, a, b))
-        sch.postprocess([(7 * i + n) % 151936 for i in ids])
+        recs.append((st.is_prefill, work * layers, a, b, n, len(st.seq_ids)))
+        eng.commit(st, [(7 * i + n) % 151936 for i in st.seq_ids])
+        del q, k, v
     torch.cuda.synchronize()
     w1 = time.perf_counter()
     assert kvp.device_status() == 0, "device status after the trace replay"
-    dec_ms = sum(a.elapsed_time(b) for p_, _, a, b in recs if not p_)
-    pre_ms = sum(a.elapsed_time(b) for p_, _, a, b in recs if p_)
-    dec_work = sum(w_ for p_, w_, _, _ in recs if not p_)
-    pre_work = sum(w_ for p_, w_, _, _ in recs if p_)
+    dec_ms = sum(a.elapsed_time(b) for p_, _, a, b, _, _ in recs if not p_)
+    pre_ms = sum(a.elapsed_time(b) for p_, _, a, b, _, _ in recs if p_)
+    dec_work = sum(w_ for p_, w_, *_ in recs if not p_)
+    pre_work = sum(w_ for p_, w_, *_ in recs if p_)
     n_dec = sum(1 for r in recs if not r[0])
-    del kv, graphs
+    # prefill steps by query tokens
+    groups = {}
+    for p_, w_, a, b, n, ns in recs:
+        if not p_:
+            continue
+        key = ">=8192 tokens" if n >= 8192 else ("1024-8191 tokens" if n >= 1024 else "<1024 tokens")
+        g = groups.setdefault(key, {"steps": 0, "tokens": 0, "seqs": 0, "ms": 0.0, "tflop": 0.0})
+        g["steps"] += 1
+        g["tokens"] += n
+        g["seqs"] += ns
+        g["ms"] += a.elapsed_time(b)
+        g["tflop"] += w_ / 1e12
+    for g in groups.values():
+        g["ms"] = round(g["ms"], 3)
+        g["tflop"] = round(g["tflop"], 4)
+        g["us_per_layer_call"] = round(g["ms"] * 1e3 / (g["steps"] * layers), 2)
+        g["tflops"] = round(g["tflop"] / (g["ms"] * 1e-3), 1)
+    preempt = eng.num_preemptions
+    del eng
     torch.cuda.empty_cache()
     dec_gbs = dec_work / (dec_ms * 1e-3) / 1e9
     pre_tf = pre_work / (pre_ms * 1e-3) / 1e12
@@ -798,16 +880,17 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
             "line": {"workload": "engine trace: 256 requests, prompts/outputs U[100,1024], 28 layers "
                                  "16/8/128, bs 256, 768 blocks, native scheduler",
                      "steps": len(recs), "decode_steps": n_dec, "prefill_steps": len(recs) - n_dec,
-                     "preemptions": sch.num_preemptions,
+                     "preemptions": preempt,
                      "decode": {"value": round(dec_gbs, 2), "unit": "GB/s", "ms": round(dec_ms, 2),
                                 "frac_of_hbm": round(dec_gbs / peaks["hbm_gbs"], 4)},
                      "prefill": {"value": round(pre_tf, 2), "unit": "TFLOP/s", "ms": round(pre_ms, 2),
-                                 "frac_of_bf16_burst": round(pre_tf / peaks["bf16_tflops"], 4)},
-                     "how": "event pair around each step's 28 layers (prefill: kv_store + "
-                            "attn_prefill_varlen, eager; decode: one copy of the packed metadata from "
-                            "pinned memory + one 28-layer graph replay of attn_decode_paged_append per "
-                            "bucket); "
-                            "inputs generated on the device before each step"}}
+                                 "frac_of_bf16_burst": round(pre_tf / peaks["bf16_tflops"], 4),
+                                 "by_query_tokens": groups},
+                     "how": "EngineReplay: event pair around each step's launch of 28 layers (prefill: "
+                            "kv_store + attn_prefill_varlen per layer, eager; decode: one copy of the "
+                            "packed metadata from pinned memory + one 28-layer graph replay of "
+                            "attn_decode_paged_append per bucket); per-layer inputs generated on the "
+                            "device before each step"}}
 
 
 def measure_scheduler():
@@ -921,12 +1004,19 @@ def run_ours(args, rank, world, local):
     time.sleep(0.3)
     windows = []
     dec = pre = None
+    if args.only == "decode_b512":  # profiling run of the large-batch decode line only
+        dl = measure_decode_large(args, kvp, W, dev, stream, world, peaks)
+        clocks = sampler.stop([dl["window"]] if dl["window"] else [])
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "only": "decode_b512", "clocks": clocks,
+                              "decode_b512": dl["line"]}), flush=True)
+        return
     if args.only != "prefill":
         dec = measure_decode(args, kvp, W, dev, stream, world, peaks)
         windows += [dec["window"], dec["uwindow"]]
     if args.only != "decode" and not args.no_prefill:
         pre = measure_prefill(args, kvp, W, dev, stream, world, peaks)
-        windows.append(pre["window"])
+        windows += [pre["window"], pre["window2"]]
     mx = None
     if args.only is None and not args.no_prefill:
         mx = measure_mixed(args, kvp, W, dev, stream, world, peaks)
@@ -935,6 +1025,10 @@ def run_ours(args, rank, world, local):
     if args.only is None:
         bk = measure_bucketed(args, kvp, W, dev, stream, world, peaks)
         windows.append(bk["window"])
+    g8 = None
+    if args.only is None:
+        g8 = measure_decode_group8(args, kvp, W, dev, stream, world, peaks)
+        windows.append(g8["window"])
     cb = None
     if args.only is None and not args.no_copy_blocks:
         cb = measure_copy_blocks(args, kvp, dev, stream, world, peaks)
@@ -976,10 +1070,11 @@ def run_ours(args, rank, world, local):
             "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
             "unfused": dec["unfused"],
             "gpu_launches": 2 * args.steps + 3 * args.steps
-                            + (0 if pre is None else 2 * pre["line"]["steps"])
+                            + (0 if pre is None else 3 * pre["line"]["steps"])
                             + (0 if cb is None else cb["line"]["steps"])
-                            + (0 if mx is None else 2 * mx["steps"])
+                            + (0 if mx is None else mx["steps"])
                             + (0 if bk is None else 2 * bk["steps"])
+                            + (0 if g8 is None else 2 * g8["steps"])
                             + (0 if dl is None else 2 * dl["steps"])
                             + (0 if tr is None else tr["launches"]),
             "gpu_launches_by_region": {"decode": {"decode_split": args.steps,
@@ -988,23 +1083,26 @@ def run_ours(args, rank, world, local):
                                                           "decode_split": args.steps,
                                                           "decode_merge": args.steps},
                                        "prefill": None if pre is None else
-                                       {"kv_store": pre["line"]["steps"],
-                                        "prefill": pre["line"]["steps"]},
+                                       {"prefill_append": pre["line"]["steps"],
+                                        "kv_store (two-call loop)": pre["line"]["steps"],
+                                        "prefill (two-call loop)": pre["line"]["steps"]},
                                        "copy_blocks": None if cb is None else
                                        {"kv_copy_blocks": cb["line"]["steps"]},
-                                       "mixed": None if mx is None else
-                                       {"kv_store": mx["steps"], "prefill": mx["steps"]},
+                                       "mixed": None if mx is None else {"prefill_append": mx["steps"]},
                                        "engine_trace": None if tr is None else {"all": tr["launches"]},
                                        "decode_b512": None if dl is None or not dl["steps"] else
                                        {"decode_split": dl["steps"], "decode_merge": dl["steps"]},
                                        "decode_bucketed": None if bk is None else
-                                       {"decode_split": bk["steps"], "decode_merge": bk["steps"]}},
+                                       {"decode_split": bk["steps"], "decode_merge": bk["steps"]},
+                                       "decode_group8": None if g8 is None else
+                                       {"decode_split": g8["steps"], "decode_merge": g8["steps"]}},
             "clocks": clocks,
             "prefill": None if pre is None else pre["line"],
             "mixed": None if mx is None else mx["line"],
             "scheduler": measure_scheduler() if args.only is None else None,
             "decode_bucketed": None if bk is None else bk["line"],
             "decode_b512": None if dl is None else dl["line"],
+            "decode_group8": None if g8 is None else g8["line"],
             "engine_trace": None if tr is None else tr["line"],
             "copy_blocks": None if cb is None else cb["line"]}
     print(json.dumps(line), flush=True)

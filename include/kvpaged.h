@@ -9,6 +9,7 @@
  *                        prefix cache (only the uncached suffix is queried)
  *   attn_decode_paged    one query token per sequence over its paged history
  *   attn_decode_paged_append  kv_store of the new rows + attn_decode_paged, fused
+ *   attn_prefill_varlen_append  kv_store of the new rows + attn_prefill_varlen, fused
  *
  * Sources: "nano-vLLM-1" (Senjl's Digital Garden), ModelRunner sections
  * "3. KV cache 分配", "4. prefill 输入打包", "5. deocde 输入打包" and BlockManager
@@ -190,6 +191,45 @@ int attn_prefill_varlen(const kvp_bf16 *q, int64_t q_stride_tok, int64_t total_q
                         const int64_t *positions, int num_heads, int num_kv_heads, int head_dim,
                         float softmax_scale, kvp_bf16 *out, int64_t out_stride_tok,
                         kvp_stream_t stream);
+
+/*
+ * attn_prefill_varlen_append - the prefill step of one layer in one launch:
+ * kv_store(k, v, slot_mapping) followed by attn_prefill_varlen.
+ *
+ * Source: "nano-vLLM-1" "4. prefill 输入打包" (slot_mapping lists the slots of
+ * the uncached tokens, one per query row; the keys of a prefix hit are read
+ * through block_tables) and "Nano vLLM 解读（5）" (the store into the KV cache
+ * comes before the attention of the same layer).
+ *
+ *   k, v            [total_q, num_kv_heads, head_dim] bf16, row stride
+ *                   kv_stride_tok (a multiple of 8 elements, 16-byte aligned):
+ *                   the new key / value of query row t
+ *   slot_mapping    [total_q] int32: cache slot of row t, -1 = no store
+ *   k_cache/v_cache written at the slots of slot_mapping; in paged mode also
+ *                   read through block_tables
+ *   block_tables    NULL: packed mode, keys/values are the rows k, v
+ *                   themselves (every k_len must equal its q_len; a sequence
+ *                   that breaks this records KVP_ERR_DEVICE_DATA and gets no
+ *                   output); else paged mode as in attn_prefill_varlen
+ *   other arguments as attn_prefill_varlen (total_k is total_q)
+ * The result is that of the two calls, for any metadata: in paged mode every
+ * CTA stores its share of the rows before any CTA loads a key tile (the
+ * launch is cooperative, one CTA per SM, and the CTAs count their stores
+ * on a device counter; a wait longer than 2 s records
+ * KVP_ERR_DEVICE_TIMEOUT), so a sequence may read, as cached prefix, rows
+ * another sequence of the same call stores.  A slot >= num_blocks *
+ * block_size stores nothing and records KVP_ERR_DEVICE_DATA.  The limit of
+ * 64 calls in flight per device is shared with attn_prefill_varlen.
+ */
+int attn_prefill_varlen_append(const kvp_bf16 *q, int64_t q_stride_tok, int64_t total_q,
+                               const kvp_bf16 *k, const kvp_bf16 *v, int64_t kv_stride_tok,
+                               const int32_t *slot_mapping, kvp_bf16 *k_cache, kvp_bf16 *v_cache,
+                               int64_t num_blocks, int block_size, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *cu_seqlens_q,
+                               const int32_t *cu_seqlens_k, int max_seqlen_q, int max_seqlen_k,
+                               int num_seqs, const int64_t *positions, int num_heads,
+                               int num_kv_heads, int head_dim, float softmax_scale, kvp_bf16 *out,
+                               int64_t out_stride_tok, kvp_stream_t stream);
 
 /*
  * Bytes of device workspace attn_decode_paged needs for this shape on the

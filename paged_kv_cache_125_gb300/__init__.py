@@ -10,6 +10,7 @@ PyTorch fallback: if the library cannot be loaded, every call raises.
     kv_store(k, v, slot_mapping, k_cache, v_cache)
     kv_copy_blocks(kv_cache, block_mapping)
     attn_prefill_varlen(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, ...)
+    attn_prefill_varlen_append(q, k, v, slot_mapping, cu_seqlens_q, cu_seqlens_k, ...)
     attn_decode_paged(q, k_cache, v_cache, block_tables, context_lens, max_context_len, ...)
 """
 from __future__ import annotations
@@ -19,8 +20,9 @@ import math
 import os
 import threading
 
-__all__ = ["kv_store", "kv_copy_blocks", "attn_prefill_varlen", "attn_decode_paged", "attn_decode_workspace_size",
-           "attn_decode_paged_noalloc", "attn_decode_paged_append",
+__all__ = ["kv_store", "kv_copy_blocks", "attn_prefill_varlen", "attn_prefill_varlen_append",
+           "attn_decode_paged", "attn_decode_workspace_size", "attn_decode_paged_noalloc",
+           "attn_decode_paged_append",
            "device_status", "selftest_wait", "library", "library_path", "KvpError"]
 
 _LIB_LOCK = threading.Lock()
@@ -49,6 +51,9 @@ SIGNATURES = {
                                          _I32, _I32, _F32, _P, _I64, _P]),
     "attn_decode_paged_append": (_I32, [_P, _I64, _P, _P, _I64, _I64, _P, _P, _P, _I64, _I32, _P, _I32,
                                         _P, _I32, _I32, _I32, _I32, _I32, _F32, _P, _SZ, _P, _I64, _P]),
+    "attn_prefill_varlen_append": (_I32, [_P, _I64, _I64, _P, _P, _I64, _P, _P, _P, _I64, _I32, _P, _I32,
+                                          _P, _P, _I32, _I32, _I32, _P, _I32, _I32, _I32, _F32, _P, _I64,
+                                          _P]),
 }
 
 
@@ -336,4 +341,50 @@ def attn_prefill_varlen(q, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_se
         _ptr(block_tables), mb,
         _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_seqlen_q), int(max_seqlen_k), nseq,
         _ptr(positions), hq, hkv, d, scale, _ptr(out), os_, _stream(q)))
+    return out
+
+
+def attn_prefill_varlen_append(q, k, v, slot_mapping, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                               max_seqlen_k: int, k_cache, v_cache, block_tables=None, positions=None,
+                               softmax_scale: float | None = None, out=None):
+    """kv_store(k, v, slot_mapping, k_cache, v_cache) followed by
+    attn_prefill_varlen, in one launch (see include/kvpaged.h).  Row t of
+    k / v is the new key / value of query row t; with block_tables the keys
+    are read from the caches (paged), without them from k / v (packed, no
+    cached prefix)."""
+    import torch
+    nb, bs, hkv, d = _cache_dims(k_cache, v_cache)
+    dev = k_cache.device
+    _require(q, "q", torch.bfloat16, 3, dev)
+    _require(k, "k", torch.bfloat16, 3, dev)
+    _require(v, "v", torch.bfloat16, 3, dev)
+    tq, hq = q.shape[0], q.shape[1]
+    qs = _rows(q, "q", hq, d)
+    kvs = _rows(k, "k", hkv, d)
+    if _rows(v, "v", hkv, d) != kvs:
+        raise ValueError("k and v must share a row stride")
+    _require(slot_mapping, "slot_mapping", torch.int32, 1, dev)
+    if k.shape[0] != tq or v.shape[0] != tq or slot_mapping.shape[0] != tq or \
+            not slot_mapping.is_contiguous():
+        raise ValueError("k, v and slot_mapping must have one (contiguous) row per query row")
+    _require(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1, dev)
+    _require(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1, dev)
+    nseq = cu_seqlens_q.shape[0] - 1
+    if cu_seqlens_k.shape[0] != nseq + 1:
+        raise ValueError("cu_seqlens_q / cu_seqlens_k lengths differ")
+    mb = 0
+    if block_tables is not None:
+        _require(block_tables, "block_tables", torch.int32, 2, dev)
+        if block_tables.shape[0] != nseq or not block_tables.is_contiguous():
+            raise ValueError("block_tables must be contiguous [num_seqs, max_blocks]")
+        mb = block_tables.shape[1]
+    if out is None:
+        out = torch.empty((tq, hq, d), dtype=torch.bfloat16, device=dev)
+    _require(out, "out", torch.bfloat16, 3, dev)
+    os_ = _rows(out, "out", hq, d)
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    _check(library().attn_prefill_varlen_append(
+        _ptr(q), qs, tq, _ptr(k), _ptr(v), kvs, _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), nb,
+        bs, _ptr(block_tables), mb, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_seqlen_q),
+        int(max_seqlen_k), nseq, _ptr(positions), hq, hkv, d, scale, _ptr(out), os_, _stream(q)))
     return out

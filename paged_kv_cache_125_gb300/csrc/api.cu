@@ -341,4 +341,54 @@ int attn_prefill_varlen(const kvp_bf16* q, int64_t q_stride_tok, int64_t total_q
   return KVP_OK;
 }
 
+int attn_prefill_varlen_append(const kvp_bf16* q, int64_t q_stride_tok, int64_t total_q,
+                               const kvp_bf16* k, const kvp_bf16* v, int64_t kv_stride_tok,
+                               const int32_t* slot_mapping, kvp_bf16* k_cache, kvp_bf16* v_cache,
+                               int64_t num_blocks, int block_size, const int32_t* block_tables,
+                               int max_blocks_per_seq, const int32_t* cu_seqlens_q,
+                               const int32_t* cu_seqlens_k, int max_seqlen_q, int max_seqlen_k,
+                               int num_seqs, const int64_t* positions, int num_heads,
+                               int num_kv_heads, int head_dim, float softmax_scale, kvp_bf16* out,
+                               int64_t out_stride_tok, kvp_stream_t stream) {
+  (void)positions;
+  const char* fn = "attn_prefill_varlen_append";
+  if (num_seqs < 0 || max_seqlen_q < 0 || max_seqlen_k < 0)
+    return fail(KVP_ERR_INVALID_ARG, "%s: bad sizes", fn);
+  if (!kvp::prefill_supported(num_heads, num_kv_heads, head_dim, block_size))
+    return fail(KVP_ERR_UNSUPPORTED, "%s: unsupported heads %d/%d, head_dim %d or block_size %d",
+                fn, num_heads, num_kv_heads, head_dim, block_size);
+  if (q_stride_tok < (int64_t)num_heads * head_dim || out_stride_tok < (int64_t)num_heads * head_dim ||
+      kv_stride_tok < (int64_t)num_kv_heads * head_dim)
+    return fail(KVP_ERR_INVALID_ARG, "%s: row stride too small", fn);
+  if (num_blocks <= 0) return fail(KVP_ERR_INVALID_ARG, "%s: num_blocks <= 0", fn);
+  if (num_blocks * (int64_t)block_size >= ((int64_t)1 << 31))
+    return fail(KVP_ERR_UNSUPPORTED, "%s: pool has 2^31 or more slots", fn);
+  if (num_seqs == 0 || max_seqlen_q == 0 || total_q == 0) return KVP_OK;
+  if (total_q < 0 || total_q >= ((int64_t)1 << 31))
+    return fail(KVP_ERR_INVALID_ARG, "%s: total_q out of range", fn);
+  if (!q || !k || !v || !slot_mapping || !k_cache || !v_cache || !cu_seqlens_q || !cu_seqlens_k ||
+      !out)
+    return fail(KVP_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (block_tables && max_blocks_per_seq <= 0)
+    return fail(KVP_ERR_INVALID_ARG, "%s: paged mode needs max_blocks_per_seq > 0", fn);
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k) || !aligned16(v) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || q_stride_tok % 8 || out_stride_tok % 8 || kv_stride_tok % 8)
+    return fail(KVP_ERR_INVALID_ARG,
+                "%s: q, k, v, caches and out need 16-byte alignment and row strides that are "
+                "multiples of 8 elements",
+                fn);
+  int dev, *status, sms;
+  int rc = device_info(&dev, &status, &sms);
+  if (rc) return rc;
+  const kvp::PrefillAppend app{k, v, kv_stride_tok, slot_mapping, k_cache, v_cache};
+  const char* why = nullptr;
+  rc = kvp::launch_prefill(q, q_stride_tok, total_q, k, v, kv_stride_tok, total_q, k_cache,
+                           v_cache, num_blocks, block_size, block_tables, max_blocks_per_seq,
+                           cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, num_seqs,
+                           num_heads, num_kv_heads, head_dim, softmax_scale, out, out_stride_tok,
+                           sms, status, (cudaStream_t)stream, &why, &app);
+  if (rc) return fail(rc, "%s: %s", fn, why ? why : "launch failed");
+  return KVP_OK;
+}
+
 }  // extern "C"

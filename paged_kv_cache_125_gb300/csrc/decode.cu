@@ -39,6 +39,8 @@
 //   takes that token's K and V row straight from the new rows (one more bulk
 //   copy) instead of from the cache, so no CTA reads a slot written in the
 //   same launch.
+#include <cudaTypedefs.h>
+
 #include <cfloat>
 
 #include "kvp_device.cuh"
@@ -86,7 +88,10 @@ __host__ __device__ constexpr int part_stride() {
   return D + 4;
 }
 
-enum : int { F_NEW = 1, F_LAST = 2, F_ENTERED = 4, F_EXITS = 8, F_DONE = 16 };
+// F_TAIL (tensor-core path with the fused store): the stage ends at the
+// sequence's last context token, whose K / V row the consumer takes from the
+// new rows instead of the cache.
+enum : int { F_NEW = 1, F_LAST = 2, F_ENTERED = 4, F_EXITS = 8, F_DONE = 16, F_TAIL = 32 };
 
 struct StageMeta {
   int b;
@@ -114,6 +119,7 @@ struct DecodeArgs {
   uint16_t* out;
   int64_t out_stride;
   int* status;
+  int tma_per_head;  // tensor-core path: one box per (kv head, panel) instead of one per stage
 };
 
 // Fused store of the new rows (null k_new: plain decode).  A kernel parameter
@@ -172,9 +178,10 @@ static_assert(decode_smem_bytes<128, 8>(ring_stages<128, 8>()) <= kSmemPerCta, "
 // Stage loop of the producer (one thread): copies the CTA's token range
 // [start, end), first sequence b0 starting at token cum0 of the batch, into
 // the ring, then posts the end marker.
-template <int D, int RS>
-__device__ void stream_stages(const DecodeArgs& a, const AppendArgs& app, uint8_t* ringK,
-                              uint8_t* ringV, StageMeta* meta, uint64_t* full, uint64_t* empty,
+template <int D, int RS, bool kTma>
+__device__ void stream_stages(const DecodeArgs& a, const AppendArgs& app, const CUtensorMap* tmK,
+                              const CUtensorMap* tmV, uint8_t* ringK, uint8_t* ringV,
+                              StageMeta* meta, uint64_t* full, uint64_t* empty,
                               long long start, long long end, int b0, long long cum0, int cap) {
   const int Hkv = a.num_kv_heads;
   a.split_seq[blockIdx.x] = -1;
@@ -217,25 +224,46 @@ __device__ void stream_stages(const DecodeArgs& a, const AppendArgs& app, uint8_
         ok = false;
         break;
       }
-      meta[s].b = b;
-      meta[s].n = n;
-      meta[s].flags = (first ? F_NEW : 0) | (t + n == t1 ? F_LAST : 0) | seg_flags;
-      const uint32_t bytes = (uint32_t)(n * row_elems * sizeof(uint16_t));
-      mbar_arrive_expect_tx(&full[s], 2 * bytes);
-      const int64_t row0 = ((int64_t)phys * a.block_size + off) * row_elems;
-      uint8_t* dk = ringK + (size_t)s * stage_half_bytes<D>();
-      uint8_t* dv = ringV + (size_t)s * stage_half_bytes<D>();
       // With the fused store, the sequence's last token comes from the new rows.
       const bool tail = app.k_new != nullptr && t + n == L;
-      const uint32_t row_bytes = (uint32_t)(row_elems * sizeof(uint16_t));
-      const uint32_t cbytes = tail ? bytes - row_bytes : bytes;
-      if (cbytes) {
-        bulk_g2s(dk, a.k_cache + row0, cbytes, &full[s]);
-        bulk_g2s(dv, a.v_cache + row0, cbytes, &full[s]);
-      }
-      if (tail) {
-        bulk_g2s(dk + cbytes, app.k_new + (int64_t)b * app.k_new_stride, row_bytes, &full[s]);
-        bulk_g2s(dv + cbytes, app.v_new + (int64_t)b * app.v_new_stride, row_bytes, &full[s]);
+      meta[s].b = b;
+      meta[s].n = n;
+      meta[s].flags = (first ? F_NEW : 0) | (t + n == t1 ? F_LAST : 0) | seg_flags |
+                      (kTma && tail ? F_TAIL : 0);
+      uint8_t* dk = ringK + (size_t)s * stage_half_bytes<D>();
+      uint8_t* dv = ringV + (size_t)s * stage_half_bytes<D>();
+      if constexpr (kTma) {
+        // One box of T rows x all heads x head_dim from the stage's first
+        // token on (rows past n are masked by the consumers); the tail row is
+        // patched in shared memory by the consumer that reads it.
+        mbar_arrive_expect_tx(&full[s], 2 * (uint32_t)stage_half_bytes<D>());
+        const int row = (int)((int64_t)phys * a.block_size + off);
+        if (!a.tma_per_head) {
+          tma_load_4d(dk, tmK, 0, row, 0, 0, &full[s]);
+          tma_load_4d(dv, tmV, 0, row, 0, 0, &full[s]);
+        } else {  // the same layout, one box {64, 1, T} per (kv head, panel)
+          const uint32_t region = (uint32_t)T * 128;
+          for (int h = 0; h < Hkv; ++h)
+            for (int p = 0; p < D / 64; ++p) {
+              const uint32_t off_b = (uint32_t)(h * (D / 64) + p) * region;
+              tma_load_3d(dk + off_b, tmK, p * 64, h, row, &full[s]);
+              tma_load_3d(dv + off_b, tmV, p * 64, h, row, &full[s]);
+            }
+        }
+      } else {
+        const uint32_t bytes = (uint32_t)(n * row_elems * sizeof(uint16_t));
+        mbar_arrive_expect_tx(&full[s], 2 * bytes);
+        const int64_t row0 = ((int64_t)phys * a.block_size + off) * row_elems;
+        const uint32_t row_bytes = (uint32_t)(row_elems * sizeof(uint16_t));
+        const uint32_t cbytes = tail ? bytes - row_bytes : bytes;
+        if (cbytes) {
+          bulk_g2s(dk, a.k_cache + row0, cbytes, &full[s]);
+          bulk_g2s(dv, a.v_cache + row0, cbytes, &full[s]);
+        }
+        if (tail) {
+          bulk_g2s(dk + cbytes, app.k_new + (int64_t)b * app.k_new_stride, row_bytes, &full[s]);
+          bulk_g2s(dv + cbytes, app.v_new + (int64_t)b * app.v_new_stride, row_bytes, &full[s]);
+        }
       }
       issued |= 1u << s;
       issued_ph = (issued_ph & ~(1u << s)) | (ph << s);
@@ -295,9 +323,10 @@ __device__ void fused_store(const DecodeArgs& a, const AppendArgs& app, int lane
   }
 }
 
-template <int D, int RS>
-__device__ void decode_producer(const DecodeArgs& a, const AppendArgs& app, uint8_t* ringK,
-                                uint8_t* ringV, StageMeta* meta, uint64_t* full, uint64_t* empty) {
+template <int D, int RS, bool kTma>
+__device__ void decode_producer(const DecodeArgs& a, const AppendArgs& app, const CUtensorMap* tmK,
+                                const CUtensorMap* tmV, uint8_t* ringK, uint8_t* ringV,
+                                StageMeta* meta, uint64_t* full, uint64_t* empty) {
   const int lane = threadIdx.x & 31;
   const int cap = a.max_blocks * a.block_size;
   const int P = gridDim.x;
@@ -346,8 +375,14 @@ __device__ void decode_producer(const DecodeArgs& a, const AppendArgs& app, uint
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
-  if (lane == 0)
-    stream_stages<D, RS>(a, app, ringK, ringV, meta, full, empty, start, end, b0, cum0, cap);
+  if (lane == 0) {
+    if constexpr (kTma) {
+      prefetch_tensormap(tmK);
+      prefetch_tensormap(tmV);
+    }
+    stream_stages<D, RS, kTma>(a, app, tmK, tmV, ringK, ringV, meta, full, empty, start, end, b0,
+                               cum0, cap);
+  }
   // The fused store, by the whole warp once every stage is issued: it overlaps
   // the consumers' last stages instead of delaying the first copies.
   __syncwarp();
@@ -743,18 +778,359 @@ __global__ void __maxnreg__(HS == 1 ? 168 : kSplitLaunchRegs) decode_split_kerne
   const int warp = threadIdx.x >> 5;
   if constexpr (HS == 1) {
     if (warp == CW)
-      decode_producer<D, RS>(a, app, ringK, ringV, meta, full, empty);
+      decode_producer<D, RS, false>(a, app, nullptr, nullptr, ringK, ringV, meta, full, empty);
     else
       decode_consumer<D, GE, HS, RS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
   } else {
     if (warp >= CW) {
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSplitProducerRegs));
-      if (warp == CW) decode_producer<D, RS>(a, app, ringK, ringV, meta, full, empty);
+      if (warp == CW)
+        decode_producer<D, RS, false>(a, app, nullptr, nullptr, ringK, ringV, meta, full, empty);
     } else {
       asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSplitConsumerRegs));
       decode_consumer<D, GE, HS, RS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
     }
   }
+}
+
+// ---------------------------------------------------------------- tensor-core consumers
+//
+// Stage layout of the tensor-core path: the producer's 4-D tensor copy lands
+// a stage half (K or V) as [kv head][64-column panel][T tokens][128 bytes]
+// with the 128-byte swizzle (16-byte chunk c of a token's 128-byte panel row
+// sits at chunk c ^ (token & 7)), so the eight token rows an ldmatrix reads
+// fall in eight different bank groups.  Every region of T rows is 1 KiB
+// aligned (T >= 8).
+//
+// A warp serves kv head g and the 8 tokens sub*8 .. sub*8+7 of every stage:
+//   S = q K^T:    mma m16n8k16, M = the G query heads of kv head g (rows G..15
+//                 zero), N = the 8 tokens, K = head_dim (D / 16 steps); the q
+//                 fragments stay in registers for the whole sequence;
+//   O^T += V^T P^T: mma m16n8k8, M = 16 columns of head_dim (D / 16 tiles),
+//                 N = 8 query heads, K = the 8 tokens.  The S accumulator of
+//                 thread (r = lane / 4, c = lane % 4) holds head r's scores
+//                 of tokens 2c, 2c + 1, which is exactly that thread's B
+//                 fragment of P^T, so P never leaves the thread; V^T comes from
+//                 transposing shared-memory loads.
+// Thread (r, c) keeps head r's running max m and row sum l (shared by the
+// quad), and O[head 2c + x][16 i + r + 8 y] in ot[i][2 y + x].  O and l are
+// rescaled only when a head's max grows by more than 2^8 (exact: O and l keep
+// the same stale reference, and P <= 2^8 fits bf16).
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// d += a b: m16n8k16, bf16 inputs, fp32 accumulate (rows 8..15 of a are zero).
+__device__ __forceinline__ void mma_k16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+// d += a b: m16n8k8, bf16 inputs, fp32 accumulate.
+__device__ __forceinline__ void mma_k8(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5}, {%6}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// Byte offset of 16-byte chunk q of token row `row` in a stage half.
+__device__ __forceinline__ uint32_t chunk_off(uint32_t region, int T, int row, int q) {
+  return region + (uint32_t)(((q >> 3) * T + row) * 128 + (((q & 7) ^ (row & 7)) << 4));
+}
+
+template <int D, int G, int RS>
+__device__ void decode_consumer_mma(const DecodeArgs& a, const AppendArgs& app,
+                                    const uint8_t* ringK, const uint8_t* ringV,
+                                    const StageMeta* meta, uint64_t* full, uint64_t* empty,
+                                    uint64_t* xfull, uint64_t* xfree, float* xw) {
+  constexpr int P = D / 64;   // 128-byte panels of a row
+  constexpr int NQ = D / 8;   // 16-byte chunks of a row
+  constexpr int KS = D / 16;  // k-steps of S; tiles of O^T
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int Hkv = a.num_kv_heads;
+  const int NS = kBaseWarps / Hkv;
+  const int g = warp % Hkv, sub = warp / Hkv;
+  const int T = kTokensAllHeads / Hkv;
+  const int head0 = g * G;
+  const int r = lane >> 2, c = lane & 3;
+  const bool srow = r < G;                    // this thread's S row is a real head
+  const bool ocol0 = 2 * c < G, ocol1 = 2 * c + 1 < G;  // its O columns are real heads
+  const uint32_t region = (uint32_t)(g * P * T * 128);
+  const int mrow = sub * 8 + (lane & 7);  // ldmatrix: lane L gives row L % 8 of matrix L / 8
+  const int msel = lane >> 3;
+  const uint32_t kbase = smem_u32(ringK), vbase = smem_u32(ringV);
+
+  uint32_t qa[KS][2];
+  float ot[KS][4];
+  float m = -INFINITY, l = 0.f;
+  int b = 0;
+  int s = 0;
+  uint32_t ph = 0;
+  int seg = 0;
+
+  while (true) {
+    if (!mbar_wait(&full[s], ph, a.status)) return;
+    const StageMeta md = meta[s];
+    if (md.flags & F_DONE) break;
+    if (md.flags & F_NEW) {
+      b = md.b;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(a.q + (int64_t)b * a.q_stride +
+                                                               (int64_t)(head0 + r) * D);
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        qa[ks][0] = srow ? qrow[ks * 8 + c] : 0u;
+        qa[ks][1] = srow ? qrow[ks * 8 + 4 + c] : 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < KS; ++i) ot[i][0] = ot[i][1] = ot[i][2] = ot[i][3] = 0.f;
+      m = -INFINITY;
+      l = 0.f;
+    }
+    const uint32_t kst = kbase + (uint32_t)(s * stage_half_bytes<D>());
+    const uint32_t vst = vbase + (uint32_t)(s * stage_half_bytes<D>());
+    const int nt = md.n - sub * 8;  // this warp's tokens in the stage (<= 0: none)
+    bool patched = false;
+    if (nt > 0) {
+      if ((md.flags & F_TAIL) && (md.n - 1) >> 3 == sub) {
+        // The sequence's last token: its row comes from the new rows (the
+        // cache slot is written in this launch).  Lanes 0..15 patch K, 16..31 V.
+        const int row = md.n - 1, q = lane & 15;
+        if (q < NQ) {
+          const uint16_t* src = (lane < 16 ? app.k_new + (int64_t)b * app.k_new_stride
+                                           : app.v_new + (int64_t)b * app.v_new_stride) +
+                                (int64_t)g * D + q * 8;
+          const uint4 u = *reinterpret_cast<const uint4*>(src);
+          const uint32_t dst = (lane < 16 ? kst : vst) + chunk_off(region, T, row, q);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(u.x), "r"(u.y),
+                       "r"(u.z), "r"(u.w)
+                       : "memory");
+        }
+        __syncwarp();
+        patched = true;
+      }
+      // S = q K^T for the warp's 8 tokens; two accumulators halve the chain.
+      float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < NQ / 4; ++j) {
+        uint32_t k0, k1, k2, k3;
+        ldsm_x4(kst + chunk_off(region, T, mrow, 4 * j + msel), k0, k1, k2, k3);
+        mma_k16(sa, qa[2 * j][0], qa[2 * j][1], k0, k1);
+        mma_k16(sb, qa[2 * j + 1][0], qa[2 * j + 1][1], k2, k3);
+      }
+      float x0 = (sa[0] + sb[0]) * a.scale_log2, x1 = (sa[1] + sb[1]) * a.scale_log2;
+      if (2 * c >= nt) x0 = -INFINITY;
+      if (2 * c + 1 >= nt) x1 = -INFINITY;
+      float mx = fmaxf(x0, x1);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      // Also the first stage of a sequence (m = -inf, alpha = 0, O still zero).
+      const bool grow = mx > m + 8.0f;
+      if (__any_sync(0xffffffffu, grow)) {
+        const float alpha = grow ? fast_exp2(m - mx) : 1.f;
+        if (grow) {
+          m = mx;
+          l *= alpha;
+        }
+        const float a0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
+        const float a1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+          ot[i][0] *= a0;
+          ot[i][1] *= a1;
+          ot[i][2] *= a0;
+          ot[i][3] *= a1;
+        }
+      }
+      const float p0 = fast_exp2(x0 - m), p1 = fast_exp2(x1 - m);
+      l += p0 + p1;
+      const uint32_t pb = pack_bf16x2(p0, p1);
+      // O^T += V^T P^T.  V rows past the warp's tokens may hold anything: zero them.
+      const uint32_t keep = 2 * c >= nt ? 0u : (2 * c + 1 >= nt ? 0x0000ffffu : 0xffffffffu);
+#pragma unroll
+      for (int j = 0; j < NQ / 4; ++j) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(vst + chunk_off(region, T, mrow, 4 * j + msel), v0, v1, v2, v3);
+        mma_k8(ot[2 * j], v0 & keep, v1 & keep, pb);
+        mma_k8(ot[2 * j + 1], v2 & keep, v3 & keep, pb);
+      }
+    }
+    if (patched) fence_proxy_async_smem();  // generic writes before the next tensor copy
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
+    if (++s == RS) {
+      s = 0;
+      ph ^= 1u;
+    }
+    if (!(md.flags & F_LAST)) continue;
+
+    // ---- end of this CTA's segment of sequence b: heads 2c, 2c + 1 of each thread
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    float mh[2] = {__shfl_sync(0xffffffffu, m, 8 * c), __shfl_sync(0xffffffffu, m, 8 * c + 4)};
+    float lh[2] = {__shfl_sync(0xffffffffu, l, 8 * c), __shfl_sync(0xffffffffu, l, 8 * c + 4)};
+    const bool oc[2] = {ocol0, ocol1};
+    bool writer = true;
+    if (NS > 1) {
+      // Warps sub > 0 of kv head g publish (O, m, l) of their heads; warp
+      // sub 0 combines them by log-sum-exp (bounded mbarrier hand-off).
+      writer = sub == 0;
+      if (!writer) {
+        if (seg > 0 && !mbar_wait(&xfree[g], (uint32_t)((seg - 1) & 1), a.status)) return;
+        float* mine = xw + (size_t)warp * G * (D + 2);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (!oc[x]) continue;
+          float* row = mine + (2 * c + x) * (D + 2);
+#pragma unroll
+          for (int i = 0; i < KS; ++i) {
+            row[16 * i + r] = ot[i][x];
+            row[16 * i + r + 8] = ot[i][2 + x];
+          }
+          if (r == 0) {
+            row[D] = mh[x];
+            row[D + 1] = lh[x];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xfull[g]);
+      } else {
+        if (!mbar_wait(&xfull[g], (uint32_t)(seg & 1), a.status)) return;
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (!oc[x]) continue;
+          float M = mh[x];
+          for (int k = 1; k < NS; ++k)
+            M = fmaxf(M, xw[(size_t)(g + k * Hkv) * G * (D + 2) + (2 * c + x) * (D + 2) + D]);
+          const float Mu = M == -INFINITY ? 0.f : M;
+          const float w0 = fast_exp2(mh[x] - Mu);
+          float ls = w0 * lh[x];
+#pragma unroll
+          for (int i = 0; i < KS; ++i) {
+            ot[i][x] *= w0;
+            ot[i][2 + x] *= w0;
+          }
+          for (int k = 1; k < NS; ++k) {
+            const float* row = xw + (size_t)(g + k * Hkv) * G * (D + 2) + (2 * c + x) * (D + 2);
+            const float w = fast_exp2(row[D] - Mu);
+            ls += w * row[D + 1];
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+              ot[i][x] += w * row[16 * i + r];
+              ot[i][2 + x] += w * row[16 * i + r + 8];
+            }
+          }
+          mh[x] = M;
+          lh[x] = ls;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xfree[g]);
+      }
+    }
+    ++seg;
+    if (!writer) continue;
+    if (!(md.flags & (F_ENTERED | F_EXITS))) {
+      // whole sequence inside this CTA: normalise and write bf16
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (!oc[x]) continue;
+        const float inv = 1.f / lh[x];
+        __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(
+            a.out + (int64_t)b * a.out_stride + (int64_t)(head0 + 2 * c + x) * D);
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+          orow[16 * i + r] = __float2bfloat16_rn(ot[i][x] * inv);
+          orow[16 * i + r + 8] = __float2bfloat16_rn(ot[i][2 + x] * inv);
+        }
+      }
+    } else {
+      const int slot = (md.flags & F_ENTERED) ? 0 : 1;
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        if (!oc[x]) continue;
+        float* dst = a.part + (((size_t)blockIdx.x * 2 + slot) * a.num_heads + head0 + 2 * c + x) *
+                                  part_stride<D>();
+#pragma unroll
+        for (int i = 0; i < KS; ++i) {
+          dst[16 * i + r] = ot[i][x];
+          dst[16 * i + r + 8] = ot[i][2 + x];
+        }
+        if (r == 0) {
+          dst[D] = mh[x];
+          dst[D + 1] = lh[x];
+        }
+      }
+    }
+  }
+}
+
+template <int D, int G>
+__host__ __device__ constexpr size_t decode_mma_smem_bytes(int ns) {
+  return 1024 + 2 * ns * stage_half_bytes<D>() + ns * sizeof(StageMeta) +
+         (2 * ns + 2 * kBaseWarps) * sizeof(uint64_t) + (size_t)kBaseWarps * G * (D + 2) * sizeof(float);
+}
+template <int D, int G>
+__host__ __device__ constexpr int mma_ring_stages() {
+  return decode_mma_smem_bytes<D, G>(kStages) <= kSmemPerCta ? kStages : kStages - 1;
+}
+static_assert(decode_mma_smem_bytes<128, 8>(mma_ring_stages<128, 8>()) <= kSmemPerCta,
+              "decode CTA smem");
+
+// The tensor-core split kernel: 8 consumer warps + 1 producer warp.  The ring
+// starts at the first 1 KiB boundary of the dynamic shared memory (the
+// swizzled tensor copies need it).
+template <int D, int G>
+__global__ void __launch_bounds__((kBaseWarps + 1) * 32, 1)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const DecodeArgs a,
+                      const AppendArgs app) {
+  constexpr int RS = mma_ring_stages<D, G>();
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* ringK = smem;
+  uint8_t* ringV = smem + RS * stage_half_bytes<D>();
+  StageMeta* meta = reinterpret_cast<StageMeta*>(smem + 2 * RS * stage_half_bytes<D>());
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + RS);
+  uint64_t* empty = full + RS;
+  uint64_t* xfull = empty + RS;
+  uint64_t* xfree = xfull + kBaseWarps;
+  float* xw = reinterpret_cast<float*>(xfree + kBaseWarps);
+
+  if (threadIdx.x == 0) {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int i = 0; i < RS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kBaseWarps);
+    }
+    const int ns = kBaseWarps / a.num_kv_heads;
+    for (int i = 0; i < kBaseWarps; ++i) {
+      mbar_init(&xfull[i], ns > 1 ? ns - 1 : 1);
+      mbar_init(&xfree[i], 1);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5;
+  if (warp == kBaseWarps)
+    decode_producer<D, RS, true>(a, app, &tmK, &tmV, ringK, ringV, meta, full, empty);
+  else
+    decode_consumer_mma<D, G, RS>(a, app, ringK, ringV, meta, full, empty, xfull, xfree, xw);
 }
 
 // Combines the partials of every sequence that crosses a CTA boundary.
@@ -854,6 +1230,96 @@ cudaError_t launch_decode_t(const DecodeArgs& a, const AppendArgs& app, int ctas
                             (const int*)a.split_seq, ctas, a.num_heads, a.out, a.out_stride);
 }
 
+// Tensor maps of one layer's K and V caches for the tensor-core path.  The
+// stage box is {64 columns, T tokens, D / 64 panels, Hkv heads} over a 4-D
+// view (column, token row, panel, head) of the [rows, Hkv, D] cache, which
+// lands a stage as [head][panel][token][64] in one copy per half; if the
+// driver does not take that view, a 3-D map (column, head, row) with a box
+// {64, 1, T} per (head, panel) gives the same layout.
+bool decode_maps(const DecodeArgs& a, int D, CUtensorMap* mk, CUtensorMap* mv, int* per_head) {
+  auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+  if (!enc) return false;
+  const int Hkv = a.num_kv_heads, T = kTokensAllHeads / Hkv;
+  const cuuint64_t rows = (cuuint64_t)a.num_blocks * a.block_size;
+  {
+    cuuint64_t dims[4] = {64, rows, (cuuint64_t)(D / 64), (cuuint64_t)Hkv};
+    cuuint64_t strides[3] = {(cuuint64_t)Hkv * D * 2, 128, (cuuint64_t)D * 2};
+    cuuint32_t box[4] = {64, (cuuint32_t)T, (cuuint32_t)(D / 64), (cuuint32_t)Hkv};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    bool ok = true;
+    for (int i = 0; i < 2 && ok; ++i)
+      ok = enc(i == 0 ? mk : mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+               const_cast<uint16_t*>(i == 0 ? a.k_cache : a.v_cache), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (ok) {
+      *per_head = 0;
+      return true;
+    }
+  }
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)T};
+  cuuint32_t es[3] = {1, 1, 1};
+  for (int i = 0; i < 2; ++i)
+    if (enc(i == 0 ? mk : mv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<uint16_t*>(i == 0 ? a.k_cache : a.v_cache), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  *per_head = 1;
+  return true;
+}
+
+cudaError_t launch_merge(const DecodeArgs& a, int D, int ctas, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas, a.num_heads);
+  cfg.blockDim = dim3(D);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (D == 128)
+    return cudaLaunchKernelEx(&cfg, decode_merge_kernel<128>, (const float*)a.part,
+                              (const int*)a.split_seq, ctas, a.num_heads, a.out, a.out_stride);
+  return cudaLaunchKernelEx(&cfg, decode_merge_kernel<64>, (const float*)a.part,
+                            (const int*)a.split_seq, ctas, a.num_heads, a.out, a.out_stride);
+}
+
+template <int D, int G>
+cudaError_t launch_decode_mma_t(DecodeArgs a, const AppendArgs& app, int ctas, cudaStream_t stream) {
+  CUtensorMap mk, mv;
+  if (!decode_maps(a, D, &mk, &mv, &a.tma_per_head)) return cudaErrorInvalidValue;
+  const size_t smem = decode_mma_smem_bytes<D, G>(mma_ring_stages<D, G>());
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_mma_kernel<D, G><<<ctas, (kBaseWarps + 1) * 32, smem, stream>>>(mk, mv, a, app);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_merge(a, D, ctas, stream);
+}
+
+// The tensor-core consumers serve every group size with the same instruction
+// count per token; the CUDA-core consumers stay for groups of one and two
+// query heads, where they stream at the HBM rate.
+template <int D, int G>
+constexpr bool use_mma() {
+  return G >= 4;
+}
+
+template <int D, int G>
+cudaError_t launch_decode_any(const DecodeArgs& a, const AppendArgs& app, int ctas,
+                              cudaStream_t stream) {
+  if constexpr (use_mma<D, G>())
+    return launch_decode_mma_t<D, G>(a, app, ctas, stream);
+  else
+    return launch_decode_t<D, G>(a, app, ctas, stream);
+}
+
 }  // namespace
 
 bool decode_supported(int num_heads, int num_kv_heads, int head_dim) {
@@ -916,20 +1382,21 @@ cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k
   a.out = out;
   a.out_stride = out_stride;
   a.status = status;
+  a.tma_per_head = 0;
   const int G = num_heads / num_kv_heads;
   if (head_dim == 128) {
     switch (G) {
-      case 1: return launch_decode_t<128, 1>(a, ap, plan.ctas, stream);
-      case 2: return launch_decode_t<128, 2>(a, ap, plan.ctas, stream);
-      case 4: return launch_decode_t<128, 4>(a, ap, plan.ctas, stream);
-      case 8: return launch_decode_t<128, 8>(a, ap, plan.ctas, stream);
+      case 1: return launch_decode_any<128, 1>(a, ap, plan.ctas, stream);
+      case 2: return launch_decode_any<128, 2>(a, ap, plan.ctas, stream);
+      case 4: return launch_decode_any<128, 4>(a, ap, plan.ctas, stream);
+      case 8: return launch_decode_any<128, 8>(a, ap, plan.ctas, stream);
     }
   } else if (head_dim == 64) {
     switch (G) {
-      case 1: return launch_decode_t<64, 1>(a, ap, plan.ctas, stream);
-      case 2: return launch_decode_t<64, 2>(a, ap, plan.ctas, stream);
-      case 4: return launch_decode_t<64, 4>(a, ap, plan.ctas, stream);
-      case 8: return launch_decode_t<64, 8>(a, ap, plan.ctas, stream);
+      case 1: return launch_decode_any<64, 1>(a, ap, plan.ctas, stream);
+      case 2: return launch_decode_any<64, 2>(a, ap, plan.ctas, stream);
+      case 4: return launch_decode_any<64, 4>(a, ap, plan.ctas, stream);
+      case 8: return launch_decode_any<64, 8>(a, ap, plan.ctas, stream);
     }
   }
   return cudaErrorInvalidValue;

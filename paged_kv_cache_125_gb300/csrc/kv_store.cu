@@ -36,28 +36,42 @@ __global__ void __launch_bounds__(kStoreThreads) kv_store_kernel(
     const int64_t t = r >> 1;
     const bool is_v = r & 1;
     const int64_t s = slots[t];
-    if (s < 0) continue;  // padding slot: nothing to write
-    if (s >= total_slots) {
-      if (lane == 0) record_error(status, KVP_ERR_DEVICE_DATA);
-      continue;
-    }
     const uint16_t* src = is_v ? v + t * v_stride : k + t * k_stride;
-    uint16_t* dst = (is_v ? v_cache : k_cache) + s * (int64_t)row_elems;
     if constexpr (kVec16) {
+      // The first four vectors per lane are loaded before the slot is known,
+      // so the data loads do not wait for the slot load.
       const int nvec = row_elems >> 3;
       const uint4* s4 = reinterpret_cast<const uint4*>(src);
-      uint4* d4 = reinterpret_cast<uint4*>(dst);
-      int i = lane;
-      for (; i + 96 < nvec; i += 128) {  // four vectors in flight per lane
-        uint4 a = ld_stream(s4 + i), b = ld_stream(s4 + i + 32), c = ld_stream(s4 + i + 64),
-              d = ld_stream(s4 + i + 96);
-        d4[i] = a;
-        d4[i + 32] = b;
-        d4[i + 64] = c;
-        d4[i + 96] = d;
+      uint4 x[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (lane + 32 * j < nvec) x[j] = ld_stream(s4 + lane + 32 * j);
+      if (s < 0) continue;  // padding slot: nothing to write
+      if (s >= total_slots) {
+        if (lane == 0) record_error(status, KVP_ERR_DEVICE_DATA);
+        continue;
       }
-      for (; i < nvec; i += 32) d4[i] = ld_stream(s4 + i);
+      uint4* d4 = reinterpret_cast<uint4*>((is_v ? v_cache : k_cache) + s * (int64_t)row_elems);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (lane + 32 * j < nvec) d4[lane + 32 * j] = x[j];
+      for (int i = lane + 128; i < nvec; i += 128) {  // rows longer than 1024 elements
+        uint4 a = ld_stream(s4 + i), b, c, d;
+        if (i + 32 < nvec) b = ld_stream(s4 + i + 32);
+        if (i + 64 < nvec) c = ld_stream(s4 + i + 64);
+        if (i + 96 < nvec) d = ld_stream(s4 + i + 96);
+        d4[i] = a;
+        if (i + 32 < nvec) d4[i + 32] = b;
+        if (i + 64 < nvec) d4[i + 64] = c;
+        if (i + 96 < nvec) d4[i + 96] = d;
+      }
     } else {
+      if (s < 0) continue;  // padding slot: nothing to write
+      if (s >= total_slots) {
+        if (lane == 0) record_error(status, KVP_ERR_DEVICE_DATA);
+        continue;
+      }
+      uint16_t* dst = (is_v ? v_cache : k_cache) + s * (int64_t)row_elems;
       for (int i = lane; i < row_elems; i += 32) dst[i] = src[i];
     }
   }

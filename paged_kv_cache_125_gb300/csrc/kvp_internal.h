@@ -65,8 +65,20 @@ cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k
                           uint16_t* out, int64_t out_stride, int* status, cudaStream_t stream,
                           const DecodeAppend* app = nullptr);
 
-// prefill.cu
+// prefill.cu: cuTensorMapEncodeTiled (a PFN_cuTensorMapEncodeTiled_v12000), or
+// null if the driver does not provide it.
+void* tensor_map_encoder();
 bool prefill_supported(int num_heads, int num_kv_heads, int head_dim, int block_size);
+// New rows of a fused store (attn_prefill_varlen_append): row t of k / v
+// (row stride `stride`) goes to slot slot_mapping[t] of the caches.
+struct PrefillAppend {
+  const uint16_t* k;
+  const uint16_t* v;
+  int64_t stride;
+  const int32_t* slot_mapping;
+  uint16_t* k_cache;
+  uint16_t* v_cache;
+};
 int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const uint16_t* k,
                    const uint16_t* v, int64_t kv_stride, int64_t total_k,
                    const uint16_t* k_cache, const uint16_t* v_cache,
@@ -74,6 +86,7 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
                    int max_blocks, const int32_t* cu_q, const int32_t* cu_k, int max_seqlen_q,
                    int max_seqlen_k, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                    float softmax_scale, uint16_t* out, int64_t out_stride, int num_sms,
-                   int* status, cudaStream_t stream, const char** why);
+                   int* status, cudaStream_t stream, const char** why,
+                   const PrefillAppend* app = nullptr);
 
 }  // namespace kvp

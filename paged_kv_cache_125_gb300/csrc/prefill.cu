@@ -98,6 +98,21 @@ struct PrefillArgs {
   uint16_t* out;
   int64_t out_stride;
   int* status;
+  // Fused store (attn_prefill_varlen_append): row t of st_k / st_v goes to
+  // slot st_slots[t] of the caches.  append 1: paged keys, the rows are
+  // stored before any K/V load (grid-wide arrival counter st_ctr); append 2:
+  // packed keys (the new rows themselves), the store needs no ordering.
+  int append;
+  int row_elems;                 // num_kv_heads * D
+  const uint16_t* st_k;
+  const uint16_t* st_v;
+  int64_t st_stride;
+  const int32_t* st_slots;
+  int64_t st_rows;               // new rows (= total_q)
+  uint16_t* k_cache_w;
+  uint16_t* v_cache_w;
+  int64_t total_slots;
+  unsigned long long* st_ctr;    // (epoch << 32) | CTAs whose rows are stored
 };
 
 struct Item {
@@ -185,7 +200,9 @@ __device__ __forceinline__ bool decode_item(const PrefillArgs& a, const Cu& cu, 
   const int ck0 = cu.k[it.b], ck1 = cu.k[it.b + 1];
   it.q_len = cq1 - cq0;
   it.k_len = ck1 - ck0;
-  if (it.q_len <= 0 || it.k_len < it.q_len) {
+  // Packed keys of the fused store are the new rows: no cached prefix.
+  const bool bad = it.k_len < it.q_len || (a.append == 2 && it.k_len != it.q_len);
+  if (it.q_len <= 0 || bad) {
     if (it.q_len > 0 && r == 0 && it.g == 0) record_error(a.status, KVP_ERR_DEVICE_DATA);
     return false;
   }
@@ -219,7 +236,7 @@ __device__ __forceinline__ bool pair_cost(const PrefillArgs& a, const Cu& cu, in
   const int r = idx / a.num_seqs, b = idx - r * a.num_seqs;
   const int q_len = cu.q[b + 1] - cu.q[b];
   const int k_len = cu.k[b + 1] - cu.k[b];
-  if (q_len <= 0 || k_len < q_len) {
+  if (q_len <= 0 || k_len < q_len || (a.append == 2 && k_len != q_len)) {
     if (q_len > 0 && r == 0) record_error(a.status, KVP_ERR_DEVICE_DATA);
     return false;
   }
@@ -378,17 +395,121 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
+// ------------------------------------------------------------------ fused store
+
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// This CTA's share of the fused store: rows [r0, r1) of the 2 x st_rows
+// (token, K-or-V) rows, each row_elems bf16 (row_elems / 8 16-byte vectors).
+// A warp copies kRows rows at a time: it first issues every slot load and
+// every 16-byte data load of those rows (a lane holds 4 vectors of each row
+// per pass over 128 vectors), then the stores, so 4 * kRows loads per lane
+// are in flight and none waits for a slot.  A negative slot stores nothing
+// (padding); a slot past the pool is reported.
+template <int kRows>
+__device__ void store_rows(const PrefillArgs& a, int warp, int nwarps, int lane) {
+  const int64_t rows = 2 * a.st_rows;
+  const int64_t r0 = rows * blockIdx.x / gridDim.x, r1 = rows * (blockIdx.x + 1) / gridDim.x;
+  const int nvec = a.row_elems >> 3;
+  for (int64_t r = r0 + (int64_t)warp * kRows; r < r1; r += (int64_t)nwarps * kRows) {
+    int64_t slot[kRows];
+    const uint4* src[kRows];
+#pragma unroll
+    for (int k = 0; k < kRows; ++k) {
+      const int64_t rr = r + k;
+      const int64_t t = rr >> 1;
+      slot[k] = rr < r1 ? (int64_t)a.st_slots[t] : -1;
+      src[k] = reinterpret_cast<const uint4*>(((rr & 1) ? a.st_v : a.st_k) + t * a.st_stride);
+    }
+    for (int jb = 0; jb < nvec; jb += 128) {
+      uint4 val[kRows][4];
+#pragma unroll
+      for (int k = 0; k < kRows; ++k)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = jb + jj * 32 + lane;
+          if (r + k < r1 && j < nvec) val[k][jj] = ld_stream16(src[k] + j);
+        }
+#pragma unroll
+      for (int k = 0; k < kRows; ++k) {
+        if (slot[k] < 0) continue;
+        if (slot[k] >= a.total_slots) {
+          if (lane == 0 && jb == 0) record_error(a.status, KVP_ERR_DEVICE_DATA);
+          continue;
+        }
+        const int64_t rr = r + k;
+        uint4* dst = reinterpret_cast<uint4*>(((rr & 1) ? a.v_cache_w : a.k_cache_w) +
+                                              slot[k] * (int64_t)a.row_elems);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = jb + jj * 32 + lane;
+          if (j < nvec) dst[j] = val[k][jj];
+        }
+      }
+    }
+  }
+}
+
+// One arrival of this CTA on the launch's store counter: (epoch << 32) |
+// arrivals.  A value still tagged with another epoch (zero after the last
+// launch on this slot reset it) is moved to this epoch first, as in
+// queue_fetch; an arrival that landed on the stale value is made again.
+__device__ __forceinline__ void store_arrive(const PrefillArgs& a) {
+  const unsigned long long v = atomicAdd(a.st_ctr, 1ull);
+  if ((uint32_t)(v >> 32) == a.epoch) return;
+  const unsigned long long fresh = (unsigned long long)a.epoch << 32;
+  unsigned long long cur = v + 1ull;
+  for (int tries = 0; (uint32_t)(cur >> 32) != a.epoch; ++tries) {
+    if (tries > 4096) {
+      record_error(a.status, KVP_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    const unsigned long long prev = atomicCAS(a.st_ctr, cur, fresh);
+    cur = prev == cur ? fresh : prev;
+  }
+  atomicAdd(a.st_ctr, 1ull);
+}
+
+// Waits (one thread, bounded) until every CTA of the launch has stored its
+// rows; then the stores are visible to this CTA's tensor copies.
+__device__ bool store_wait(const PrefillArgs& a) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.st_ctr) : "memory");
+    if ((uint32_t)(v >> 32) == a.epoch && (uint32_t)v >= gridDim.x) break;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      record_error(a.status, KVP_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
+}
+
 // ------------------------------------------------------------------ producer
 
 template <int D>
 __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, const CUtensorMap* tmK,
-                              const CUtensorMap* tmV, uint8_t* smem, uint64_t* bars, Sched* sc) {
+                              const CUtensorMap* tmV, const CUtensorMap* tmKn,
+                              const CUtensorMap* tmVn, uint8_t* smem, uint64_t* bars, Sched* sc) {
   using Lay = Layout<D>;
   const int lane = threadIdx.x & 31;
   if (lane == 0) {
     prefetch_tensormap(tmQ);
     prefetch_tensormap(tmK);
     prefetch_tensormap(tmV);
+    if (a.append == 1) {
+      prefetch_tensormap(tmKn);
+      prefetch_tensormap(tmVn);
+    }
   }
   if (a.dynamic) build_order(a, sc);
   const Cu cu = cu_view(a, sc);
@@ -403,6 +524,7 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
   int next_pos = blockIdx.x, rr = 0;
   int item_idx = 0;
   uint32_t jt = 0;
+  bool stored = false;
   Item it;
   for (;; ++item_idx) {
     bool have = false;
@@ -461,9 +583,18 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
       int rowi[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) rowi[i] = 0;
+      uint32_t from_new = 0;  // fused store: sub-boxes read from the new rows
+      bool reads_cache = false;
       if (a.paged) {
         for (int i = 0; i < nsub; ++i) {
           const int key = key0 + i * rows_per_box;
+          if (a.append == 1 && key >= it.cached) {
+            // Entirely in the uncached suffix: the new rows hold these keys.
+            from_new |= 1u << i;
+            rowi[i] = it.q_row0 - it.q0 + (key - it.cached);
+            continue;
+          }
+          reads_cache = true;
           const int lb = key / a.block_size;
           const int wb = lb & ~31;
           if (wb != win_base) {  // warp-uniform
@@ -481,6 +612,13 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
       } else {
         rowi[0] = it.k_row0 + key0;
       }
+      if (reads_cache && a.append == 1 && !stored) {
+        // A cache read: every CTA's share of the fused store must have landed.
+        int ok = 1;
+        if (lane == 0) ok = store_wait(a) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+        stored = true;
+      }
       for (int kv = 0; kv < 2; ++kv) {
         const int full = kv == 0 ? B_KFULL : B_VFULL;
         const int empty = kv == 0 ? B_KEMPTY : B_VEMPTY;
@@ -488,11 +626,13 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars[full + st], bytes);
           uint8_t* dst = smem + (kv == 0 ? Lay::kK : Lay::kV) + st * Lay::kKVBytes;
-          const CUtensorMap* map = kv == 0 ? tmK : tmV;
-          for (int i = 0; i < nsub; ++i)
+          for (int i = 0; i < nsub; ++i) {
+            const CUtensorMap* map = (from_new >> i & 1u) ? (kv == 0 ? tmKn : tmVn)
+                                                          : (kv == 0 ? tmK : tmV);
             for (int p = 0; p < (int)Lay::kPanels; ++p)
               tma_load_3d(dst + p * Lay::kPanelBytes + i * rows_per_box * 128, map, p * 64, it.g,
                           rowi[i], &bars[full + st]);
+          }
         }
       }
     }
@@ -799,7 +939,8 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
 template <int D>
 __global__ void __launch_bounds__(kThreadsPF, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmKn,
+                   const __grid_constant__ CUtensorMap tmVn, const PrefillArgs a) {
   using Lay = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {  // the 128-byte swizzle needs a 1 KiB aligned base
@@ -844,13 +985,26 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
     if (warp == kProducerWarp)
-      producer_role<D>(a, &tmQ, &tmK, &tmV, smem, bars, sc);
+      producer_role<D>(a, &tmQ, &tmK, &tmV, &tmKn, &tmVn, smem, bars, sc);
     else if (warp == kMmaWarp && (threadIdx.x & 31) == 0)
       mma_role<D>(a, smem, bars, tbase, sc);
     else if (warp == kVFixWarp)
       vfix_role<D>(a, smem, bars, sc);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+    if (a.append) {
+      // The fused store, by the softmax warps while the control warps set up
+      // the first item (their first S needs a K tile that comes after it).
+      store_rows<4>(a, threadIdx.x >> 5, 8, threadIdx.x & 31);
+      if (a.append == 1) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        named_barrier_sync(1, 256);
+        if (threadIdx.x == 0) {
+          __threadfence();
+          store_arrive(a);
+        }
+      }
+    }
     softmax_role<D>(a, smem, bars, tbase, sc);
   }
 
@@ -858,13 +1012,14 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tbase, 512);
-  if (a.dynamic && threadIdx.x == 0) {
-    // Every fetch of this CTA is done.  The last CTA to get here returns the
-    // counter slot to zero, so the same launch parameters (a CUDA graph
-    // replay) start from position 0 again.
+  if ((a.dynamic || a.append == 1) && threadIdx.x == 0) {
+    // Every fetch and store wait of this CTA is done.  The last CTA to get
+    // here returns the counter slot to zero, so the same launch parameters (a
+    // CUDA graph replay) start from position 0 again.
     __threadfence();
     if (atomicAdd(a.qdone, 1u) == gridDim.x - 1) {
       atomicExch(a.qslot, 0ull);
+      if (a.st_ctr) atomicExch(a.st_ctr, 0ull);
       atomicExch(a.qdone, 0u);
     }
   }
@@ -874,6 +1029,7 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
 // (launch n uses slot n % kQueueSlots with epoch n / kQueueSlots + 1).
 __device__ unsigned long long g_queue_slot[kQueueSlots];
 __device__ unsigned int g_queue_done[kQueueSlots];
+__device__ unsigned long long g_store_ctr[kQueueSlots];  // fused store: arrivals per launch
 
 // ------------------------------------------------------------------ host side
 
@@ -882,10 +1038,18 @@ __device__ unsigned int g_queue_done[kQueueSlots];
 constexpr int kMaxQueueDevices = 64;
 unsigned long long* g_qslot_ptr[kMaxQueueDevices];
 unsigned int* g_qdone_ptr[kMaxQueueDevices];
+unsigned long long* g_stctr_ptr[kMaxQueueDevices];
 std::atomic<unsigned long long> g_qseq[kMaxQueueDevices];
 std::mutex g_queue_mutex;
 
-bool queue_slots(unsigned long long** slots, unsigned int** dones, unsigned long long* seq) {
+struct QueueSlot {
+  unsigned long long* next;   // dynamic schedule counter
+  unsigned int* done;         // CTAs finished
+  unsigned long long* store;  // fused store arrivals
+  uint32_t epoch;
+};
+
+bool queue_slot(QueueSlot* q) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxQueueDevices) return false;
   {
@@ -893,16 +1057,21 @@ bool queue_slots(unsigned long long** slots, unsigned int** dones, unsigned long
     if (!g_qslot_ptr[dev]) {
       void* ps = nullptr;
       void* pd = nullptr;
+      void* pc = nullptr;
       if (cudaGetSymbolAddress(&ps, g_queue_slot) != cudaSuccess ||
-          cudaGetSymbolAddress(&pd, g_queue_done) != cudaSuccess)
+          cudaGetSymbolAddress(&pd, g_queue_done) != cudaSuccess ||
+          cudaGetSymbolAddress(&pc, g_store_ctr) != cudaSuccess)
         return false;
       g_qdone_ptr[dev] = static_cast<unsigned int*>(pd);
+      g_stctr_ptr[dev] = static_cast<unsigned long long*>(pc);
       g_qslot_ptr[dev] = static_cast<unsigned long long*>(ps);
     }
   }
-  *slots = g_qslot_ptr[dev];
-  *dones = g_qdone_ptr[dev];
-  *seq = g_qseq[dev].fetch_add(1);
+  const unsigned long long seq = g_qseq[dev].fetch_add(1);
+  q->next = g_qslot_ptr[dev] + seq % kQueueSlots;
+  q->done = g_qdone_ptr[dev] + seq % kQueueSlots;
+  q->store = g_stctr_ptr[dev] + seq % kQueueSlots;
+  q->epoch = (uint32_t)(seq / kQueueSlots) + 1u;
   return true;
 }
 
@@ -935,18 +1104,37 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, 
          CUDA_SUCCESS;
 }
 
+// A launch whose CTAs wait for each other (the fused store before paged
+// loads) is cooperative: it fails to launch instead of running with CTAs that
+// cannot all be resident (one CTA per SM, grid <= SMs).
 template <int D>
 cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
-                     const PrefillArgs& a, int grid, cudaStream_t stream) {
+                     const CUtensorMap& kn, const CUtensorMap& vn, const PrefillArgs& a, int grid,
+                     cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Layout<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  prefill_kernel<D><<<grid, kThreadsPF, Layout<D>::kAlloc, stream>>>(q, k, v, a);
-  return cudaGetLastError();
+  if (a.append != 1) {
+    prefill_kernel<D><<<grid, kThreadsPF, Layout<D>::kAlloc, stream>>>(q, k, v, kn, vn, a);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreadsPF);
+  cfg.dynamicSmemBytes = Layout<D>::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, prefill_kernel<D>, q, k, v, kn, vn, a);
 }
 
 }  // namespace
+
+void* tensor_map_encoder() { return get_encoder() ? reinterpret_cast<void*>(g_encode) : nullptr; }
 
 bool prefill_supported(int num_heads, int num_kv_heads, int head_dim, int block_size) {
   if (num_kv_heads <= 0 || num_heads <= 0 || num_heads % num_kv_heads) return false;
@@ -965,7 +1153,8 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
                    const int32_t* cu_q, const int32_t* cu_k, int max_seqlen_q, int max_seqlen_k,
                    int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                    float softmax_scale, uint16_t* out, int64_t out_stride, int num_sms,
-                   int* status, cudaStream_t stream, const char** why) {
+                   int* status, cudaStream_t stream, const char** why,
+                   const PrefillAppend* app) {
   (void)max_seqlen_k;
   if (!get_encoder()) {
     *why = "cuTensorMapEncodeTiled is unavailable";
@@ -975,7 +1164,7 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
   const int tok = kBM / G;
   const bool paged = block_tables != nullptr;
   const int sub_rows = paged ? (block_size < kBN ? block_size : kBN) : kBN;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mkn, mvn;
   bool ok = make_map(&mq, q, total_q, num_heads, head_dim, q_stride, G, tok);
   if (paged) {
     const int64_t rows = num_blocks * (int64_t)block_size;
@@ -986,9 +1175,16 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
     ok = ok && make_map(&mk, k, total_k, num_kv_heads, head_dim, kv_stride, 1, kBN) &&
          make_map(&mv, v, total_k, num_kv_heads, head_dim, kv_stride, 1, kBN);
   }
+  if (ok && paged && app)  // the fused store's new rows, read for uncached keys
+    ok = make_map(&mkn, app->k, total_q, num_kv_heads, head_dim, app->stride, 1, sub_rows) &&
+         make_map(&mvn, app->v, total_q, num_kv_heads, head_dim, app->stride, 1, sub_rows);
   if (!ok) {
     *why = "tensor map encoding failed (alignment or extent)";
     return KVP_ERR_INVALID_ARG;
+  }
+  if (!(paged && app)) {
+    mkn = mk;
+    mvn = mv;
   }
   PrefillArgs a;
   a.cu_q = cu_q;
@@ -1019,21 +1215,40 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
   a.qslot = nullptr;
   a.qdone = nullptr;
   a.epoch = 0;
-  if (a.dynamic) {
-    unsigned long long* slots;
-    unsigned int* dones;
-    unsigned long long seq;
-    if (!queue_slots(&slots, &dones, &seq)) {
-      *why = "counter slots of the dynamic schedule unavailable";
+  a.append = 0;
+  a.row_elems = num_kv_heads * head_dim;
+  a.st_k = a.st_v = nullptr;
+  a.st_stride = 0;
+  a.st_slots = nullptr;
+  a.st_rows = 0;
+  a.k_cache_w = a.v_cache_w = nullptr;
+  a.total_slots = 0;
+  a.st_ctr = nullptr;
+  if (app) {
+    a.append = paged ? 1 : 2;
+    a.st_k = app->k;
+    a.st_v = app->v;
+    a.st_stride = app->stride;
+    a.st_slots = app->slot_mapping;
+    a.st_rows = total_q;
+    a.k_cache_w = app->k_cache;
+    a.v_cache_w = app->v_cache;
+    a.total_slots = num_blocks * (int64_t)block_size;
+  }
+  if (a.dynamic || a.append == 1) {
+    QueueSlot qs;
+    if (!queue_slot(&qs)) {
+      *why = "counter slots of the launch unavailable";
       return KVP_ERR_CUDA;
     }
-    a.qslot = slots + seq % kQueueSlots;
-    a.qdone = dones + seq % kQueueSlots;
-    a.epoch = (uint32_t)(seq / kQueueSlots) + 1u;
+    a.qslot = qs.next;
+    a.qdone = qs.done;
+    a.st_ctr = a.append == 1 ? qs.store : nullptr;
+    a.epoch = qs.epoch;
   }
   a.cu_in_smem = num_seqs + 1 <= kCuCap ? 1 : 0;
-  cudaError_t e = head_dim == 128 ? launch_t<128>(mq, mk, mv, a, grid, stream)
-                                  : launch_t<64>(mq, mk, mv, a, grid, stream);
+  cudaError_t e = head_dim == 128 ? launch_t<128>(mq, mk, mv, mkn, mvn, a, grid, stream)
+                                  : launch_t<64>(mq, mk, mv, mkn, mvn, a, grid, stream);
   if (e != cudaSuccess) {
     *why = cudaGetErrorString(e);
     return KVP_ERR_CUDA;

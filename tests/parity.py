@@ -63,10 +63,11 @@ def gpu_pool(w: W.Workload, device="cuda"):
     return kc, vc
 
 
-def run_gpu(w: W.Workload, device="cuda", fused_decode=False):
+def run_gpu(w: W.Workload, device="cuda", fused_decode=False, fused_prefill=False):
     """-> (per-step bf16 outputs on the device, k_cache, v_cache).  With
     fused_decode, decode steps go through attn_decode_paged_append (store and
-    attention in one launch) instead of kv_store + attn_decode_paged."""
+    attention in one launch) instead of kv_store + attn_decode_paged; with
+    fused_prefill, prefill steps through attn_prefill_varlen_append."""
     kc, vc = gpu_pool(w, device)
     for st in w.setup:
         kvp.kv_store(st.k.to(device), st.v.to(device), st.slot_mapping.to(device), kc, vc)
@@ -80,6 +81,13 @@ def run_gpu(w: W.Workload, device="cuda", fused_decode=False):
                 a.q.to(device), s.k.to(device), s.v.to(device), s.slot_mapping.to(device), kc, vc,
                 m.block_tables.to(device), m.context_lens.to(device), m.max_context_len,
                 softmax_scale=w.scale))
+            continue
+        if fused_prefill and step.is_prefill:
+            bt = None if m.block_tables is None else m.block_tables.to(device)
+            outs.append(kvp.attn_prefill_varlen_append(
+                a.q.to(device), s.k.to(device), s.v.to(device), s.slot_mapping.to(device),
+                m.cu_seqlens_q.to(device), m.cu_seqlens_k.to(device), m.max_seqlen_q, m.max_seqlen_k,
+                kc, vc, block_tables=bt, softmax_scale=w.scale))
             continue
         kvp.kv_store(s.k.to(device), s.v.to(device), s.slot_mapping.to(device), kc, vc)
         if step.is_prefill:

@@ -155,3 +155,32 @@ def test_decode_append_validation(lib):
     assert _append(lib, b=4, slots=None) == INVALID and "null" in _err(lib)
     assert _append(lib, b=4, k=MIS) == INVALID and "alignment" in _err(lib)
     assert _append(lib, b=4, vs=8 * 128 + 4) == INVALID
+
+
+def _prefill_append(lib, **kw):
+    a = dict(q=A, q_stride=32 * 128, tq=16, k=A, v=A, kv_stride=8 * 128, slots=A, kc=A, vc=A, nb=64,
+             bs=256, bt=A, mb=16, cq=A, ck=A, mq=16, mk=16, b=1, hq=32, hkv=8, d=128, out=A,
+             out_stride=32 * 128)
+    a.update(kw)
+    return lib.attn_prefill_varlen_append(a["q"], a["q_stride"], a["tq"], a["k"], a["v"], a["kv_stride"],
+                                          a["slots"], a["kc"], a["vc"], a["nb"], a["bs"], a["bt"], a["mb"],
+                                          a["cq"], a["ck"], a["mq"], a["mk"], a["b"], None, a["hq"],
+                                          a["hkv"], a["d"], 0.088, a["out"], a["out_stride"], None)
+
+
+def test_prefill_append_validation(lib):
+    assert _prefill_append(lib, b=0) == OK            # no sequences: a no-op
+    assert _prefill_append(lib, tq=0) == OK           # no query rows: a no-op
+    assert _prefill_append(lib, b=-1) == INVALID and "bad sizes" in _err(lib)
+    assert _prefill_append(lib, hq=24) == UNSUPPORTED and "attn_prefill_varlen_append" in _err(lib)
+    assert _prefill_append(lib, bs=48) == UNSUPPORTED
+    assert _prefill_append(lib, kv_stride=8 * 128 - 8) == INVALID and "stride" in _err(lib)
+    assert _prefill_append(lib, nb=0) == INVALID and "num_blocks" in _err(lib)
+    assert _prefill_append(lib, nb=1 << 24) == UNSUPPORTED and "2^31" in _err(lib)
+    assert _prefill_append(lib, tq=-3) == INVALID and "total_q" in _err(lib)
+    for name in ("q", "k", "v", "slots", "kc", "vc", "cq", "ck", "out"):
+        assert _prefill_append(lib, **{name: None}) == INVALID and "null" in _err(lib), name
+    assert _prefill_append(lib, mb=0) == INVALID and "max_blocks_per_seq" in _err(lib)
+    for name in ("q", "k", "v", "kc", "vc", "out"):
+        assert _prefill_append(lib, **{name: MIS}) == INVALID and "16-byte" in _err(lib), name
+    assert _prefill_append(lib, kv_stride=8 * 128 + 4) == INVALID and "multiples of 8" in _err(lib)
