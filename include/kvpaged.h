@@ -212,14 +212,15 @@ int attn_prefill_varlen(const kvp_bf16 *q, int64_t q_stride_tok, int64_t total_q
  *                   that breaks this records KVP_ERR_DEVICE_DATA and gets no
  *                   output); else paged mode as in attn_prefill_varlen
  *   other arguments as attn_prefill_varlen (total_k is total_q)
- * The result is that of the two calls, for any metadata: in paged mode every
- * CTA stores its share of the rows before any CTA loads a key tile (the
- * launch is cooperative, one CTA per SM, and the CTAs count their stores
- * on a device counter; a wait longer than 2 s records
- * KVP_ERR_DEVICE_TIMEOUT), so a sequence may read, as cached prefix, rows
- * another sequence of the same call stores.  A slot >= num_blocks *
- * block_size stores nothing and records KVP_ERR_DEVICE_DATA.  The limit of
- * 64 calls in flight per device is shared with attn_prefill_varlen.
+ * The result is that of the two calls, for any metadata.  The call enqueues
+ * a store grid on at most half of the SMs and the prefill as its
+ * programmatic dependent: the prefill starts on the other SMs at once, takes
+ * each sequence's uncached key tiles first (read from k / v, which hold
+ * them) and waits for the store grid before its first read of the cache, so
+ * a sequence may read, as cached prefix, rows another sequence of the same
+ * call stores.  A slot >= num_blocks * block_size stores nothing and records
+ * KVP_ERR_DEVICE_DATA.  The limit of 64 calls in flight per device is shared
+ * with attn_prefill_varlen.
  */
 int attn_prefill_varlen_append(const kvp_bf16 *q, int64_t q_stride_tok, int64_t total_q,
                                const kvp_bf16 *k, const kvp_bf16 *v, int64_t kv_stride_tok,

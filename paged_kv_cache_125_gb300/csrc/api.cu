@@ -380,7 +380,12 @@ int attn_prefill_varlen_append(const kvp_bf16* q, int64_t q_stride_tok, int64_t 
   int dev, *status, sms;
   int rc = device_info(&dev, &status, &sms);
   if (rc) return rc;
-  const kvp::PrefillAppend app{k, v, kv_stride_tok, slot_mapping, k_cache, v_cache};
+  cudaError_t e = kvp::launch_kv_store_narrow(k, v, kv_stride_tok, slot_mapping, total_q, k_cache,
+                                              v_cache, num_blocks * (int64_t)block_size,
+                                              num_kv_heads * head_dim, sms, status,
+                                              (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "attn_prefill_varlen_append store launch");
+  const kvp::PrefillAppend app{k, v, kv_stride_tok};
   const char* why = nullptr;
   rc = kvp::launch_prefill(q, q_stride_tok, total_q, k, v, kv_stride_tok, total_q, k_cache,
                            v_cache, num_blocks, block_size, block_tables, max_blocks_per_seq,

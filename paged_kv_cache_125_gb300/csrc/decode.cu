@@ -22,23 +22,29 @@
 //   (cp.async.bulk + mbarrier transaction counts); it reads the block table as
 //   it goes, so the gather costs nothing beyond the copy addresses.
 // * Eight consumer warps; warp w serves kv head w % Hkv (and, when
-//   Hkv < 8, token subset w / Hkv).  A lane owns 1/8 of head_dim (two 16-byte
-//   chunks at head_dim 128) of one token; 4 tokens per pass.  q . k is an
-//   fp32 dot product over the lane's slice reduced over 8 lanes by shuffles,
-//   with q pre-scaled by softmax_scale * log2(e) so the softmax uses exp2.
-//   The running max is warp-uniform and updated once per stage.  Where
-//   G * head_dim >= 512 the query heads of a kv head are split over two
-//   warps (16 consumer warps, see head_split), the producer gets a warpgroup
-//   of its own that hands registers to the consumers (setmaxnreg), and the
-//   score reduction runs on pairs of heads.
+//   Hkv < 8, tokens (w / Hkv) * 8 .. + 7 of each stage, or the token subset
+//   w / Hkv).  Two kinds of consumers:
+//   - one or two query heads per kv head (CUDA cores): a lane owns 1/8 of
+//     head_dim (two 16-byte chunks at head_dim 128) of one token; 4 tokens
+//     per pass.  q . k is an fp32 dot product over the lane's slice reduced
+//     over 8 lanes by shuffles, with q pre-scaled by softmax_scale * log2(e)
+//     so the softmax uses exp2.  The running max is warp-uniform and updated
+//     once per stage.  These stream at the HBM rate.
+//   - four or eight query heads per kv head (tensor cores, mma.sync): the
+//     stage is copied by one 4-D tensor copy per half into a swizzled
+//     [head][panel][token][64] layout; S = q K^T and O^T = V^T P^T are
+//     m16n8k16 / m16n8k8 MMAs over the warp's 8 tokens (see the section
+//     "tensor-core consumers" below).  The CUDA-core form needs 2 FMAs per
+//     K/V byte at G = 4 and is issue-bound there.
 // * Optional store of the step's new rows (attn_decode_paged_append): the
 //   kv_store of one new token per sequence is folded into the same launch.
 //   After the producer has issued every stage, its warp writes the rows of
 //   sequences i, i + P, ... (CTA i) into the cache slots slot_mapping[b];
 //   the stage that ends at a sequence's last context token
 //   takes that token's K and V row straight from the new rows (one more bulk
-//   copy) instead of from the cache, so no CTA reads a slot written in the
-//   same launch.
+//   copy; on the tensor-core path the consumer writes that row into the
+//   swizzled stage) instead of from the cache, so no CTA reads a slot written
+//   in the same launch.
 #include <cudaTypedefs.h>
 
 #include <cfloat>
@@ -48,38 +54,11 @@
 namespace kvp {
 namespace {
 
-constexpr int kBaseWarps = 8;  // consumer warps before the head split
-constexpr int kStages = 6;  // ring depth (one less where the CTA would not fit, see ring_stages)
+constexpr int kBaseWarps = 8;  // consumer warps
+constexpr int kStages = 6;  // ring depth (one less where a tensor-core CTA would not fit)
 constexpr size_t kSmemPerCta = 227 * 1024;
 
-// Query heads of a kv head are split over HS warps when a warp holding all
-// G of them would need G * D / 8 query floats plus as many accumulators per
-// lane (G * D >= 512): each warp then owns G / HS heads, so its query and
-// accumulators stay in registers and twice as many warps hide the latency of
-// the dot products.  HS = 2 gives 16 consumer warps + the producer: 17 warps,
-// 5 on one SM sub-partition, so at most 16384 / (5 * 32) = 102 registers.
-template <int D, int G>
-__host__ __device__ constexpr int head_split() {
-  return G * D >= 512 ? 2 : 1;
-}
-template <int HS>
-__host__ __device__ constexpr int consumer_warps() {
-  return kBaseWarps * HS;
-}
 constexpr int kTokensAllHeads = 64;  // tokens * kv heads per stage
-
-// With the head split the producer gets a warpgroup of its own (warps CW ..
-// CW + 3; only the first works) so that setmaxnreg can move registers from it
-// to the consumers: the launch gives 20 warps x 96 registers; the producer
-// group keeps 32 and the 16 consumer warps take 112, enough for their q slices
-// and accumulators without spilling.
-template <int HS>
-__host__ __device__ constexpr int block_warps() {
-  return HS == 1 ? consumer_warps<HS>() + 1 : consumer_warps<HS>() + 4;
-}
-constexpr int kSplitLaunchRegs = 96, kSplitConsumerRegs = 112, kSplitProducerRegs = 32;
-static_assert(16 * 32 * kSplitConsumerRegs + 4 * 32 * kSplitProducerRegs <= 20 * 32 * kSplitLaunchRegs,
-              "register split exceeds the launch's allotment");
 
 // Row of one split partial in the workspace: accumulator[D], m, l, and two pad
 // floats so that every row starts on a 16-byte boundary (float4 stores).
@@ -147,31 +126,17 @@ __host__ __device__ constexpr size_t stage_half_bytes() {
   return (size_t)kTokensAllHeads * D * sizeof(uint16_t);
 }
 
+// CUDA-core path (one or two query heads per kv head): the ring, the stage
+// records, the ring and hand-off barriers and each warp's partial staging.
 // With 9 warps per CTA one SM sub-partition runs 3 of them, so a thread can
-// hold at most 168 registers.  When the scaled query slice of a lane (G * D / 8
-// floats) plus the accumulators would not fit, the query lives in shared
-// memory (per warp, fp32) and is read with broadcast loads.
-template <int D, int G>
-__host__ __device__ constexpr bool q_in_smem() {
-  return G * D >= 512;
-}
-
+// hold at most 168 registers: a lane's query slice (G * D / 8 floats) and
+// accumulators fit.
 template <int D, int G>
 __host__ __device__ constexpr size_t decode_smem_bytes(int ns) {
-  constexpr int HS = head_split<D, G>(), CW = consumer_warps<HS>(), GE = G / HS;
   return 2 * ns * stage_half_bytes<D>() + ns * sizeof(StageMeta) +
-         (2 * ns + 2 * CW) * sizeof(uint64_t) + (size_t)CW * GE * (D + 2) * sizeof(float) +
-         (q_in_smem<D, GE>() ? (size_t)CW * GE * D * sizeof(float) : 0);
+         (2 * ns + 2 * kBaseWarps) * sizeof(uint64_t) + (size_t)kBaseWarps * G * (D + 2) * sizeof(float);
 }
-
-// Stages of the K/V ring: kStages, or one less where the head split's query
-// and partial staging would take the CTA past 227 KiB (G * D = 1024: eight
-// query heads per kv head at head_dim 128).
-template <int D, int G>
-__host__ __device__ constexpr int ring_stages() {
-  return decode_smem_bytes<D, G>(kStages) <= kSmemPerCta ? kStages : kStages - 1;
-}
-static_assert(decode_smem_bytes<128, 8>(ring_stages<128, 8>()) <= kSmemPerCta, "decode CTA smem");
+static_assert(decode_smem_bytes<128, 2>(kStages) <= kSmemPerCta, "decode CTA smem");
 
 // ---------------------------------------------------------------- producer
 
@@ -391,39 +356,23 @@ __device__ void decode_producer(const DecodeArgs& a, const AppendArgs& app, cons
 
 // ---------------------------------------------------------------- consumers
 
-// Template G here is the number of query heads this warp owns (the group
-// size divided by the head split HS); hs selects which part of the group.
-template <int D, int G, int HS, int RS>
+// The CUDA-core consumers (G = 1 or 2 query heads per kv head).
+template <int D, int G, int RS>
 __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const uint8_t* ringV,
                                 const StageMeta* meta, uint64_t* full, uint64_t* empty,
-                                uint64_t* xfull, uint64_t* xfree, float* xw, float* qs_all) {
+                                uint64_t* xfull, uint64_t* xfree, float* xw) {
   constexpr int NCH = D / 64;  // 16-byte chunks of one row per lane
-  constexpr bool kQS = q_in_smem<D, G>();
-  // Heads in pairs (2q, 2q+1): the first level of the 8-lane score reduction
-  // hands head 2q to the lanes with bit 2 of li clear and head 2q+1 to the
-  // others, so the other two levels, the running max and the exponentials run
-  // once per pair instead of once per head.  Used where the head split makes
-  // the warps issue-bound (32/8/128: 341 -> 324 us on a 128-sequence batch);
-  // at G = 2 without the split the stream is HBM-bound and the extra
-  // shuffles on the score path cost 2%.
-  constexpr bool kPair = HS == 2 && G % 2 == 0;
-  constexpr int GP = kPair ? G / 2 : 1;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = a.num_kv_heads;
   const int NS = kBaseWarps / Hkv;
-  const int hs = warp % HS, wb = warp / HS;
-  const int g = wb % Hkv, sub = wb / Hkv;
-  const int head0 = (g * HS + hs) * G;  // first query head of this warp
-  const int xi = g * HS + hs;           // hand-off barriers of (kv head, head part)
+  const int g = warp % Hkv, sub = warp / Hkv;
+  const int head0 = g * G;  // first query head of this warp
   const int li = lane & 7, tg = lane >> 3;
   const int row_elems = Hkv * D;
 
-  // Scaled query: registers, or this warp's [G][D] fp32 slice of shared memory.
-  float qf[kQS ? 1 : G][NCH][8];
-  float* qs = qs_all + (size_t)warp * G * D;
+  float qf[G][NCH][8];  // scaled query
   float acc[G][NCH][8];
   float m[G], l[G];
-  float mo[GP], lo[GP];  // paired heads: running max and sum of this lane's head of each pair
   int b = 0;
   int s = 0;
   uint32_t ph = 0;
@@ -443,20 +392,10 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
         for (int c = 0; c < NCH; ++c) {
           const uint4 u = *reinterpret_cast<const uint4*>(qrow + h * D + (c * 8 + li) * 8);
           const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-          if constexpr (kQS) {
-            if (tg == 0) {
-              float4* d4 = reinterpret_cast<float4*>(qs + h * D + (c * 8 + li) * 8);
-              d4[0] = make_float4(bf16lo(w[0]) * a.scale_log2, bf16hi(w[0]) * a.scale_log2,
-                                  bf16lo(w[1]) * a.scale_log2, bf16hi(w[1]) * a.scale_log2);
-              d4[1] = make_float4(bf16lo(w[2]) * a.scale_log2, bf16hi(w[2]) * a.scale_log2,
-                                  bf16lo(w[3]) * a.scale_log2, bf16hi(w[3]) * a.scale_log2);
-            }
-          } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              qf[h][c][2 * e] = bf16lo(w[e]) * a.scale_log2;
-              qf[h][c][2 * e + 1] = bf16hi(w[e]) * a.scale_log2;
-            }
+          for (int e = 0; e < 4; ++e) {
+            qf[h][c][2 * e] = bf16lo(w[e]) * a.scale_log2;
+            qf[h][c][2 * e + 1] = bf16hi(w[e]) * a.scale_log2;
           }
 #pragma unroll
           for (int e = 0; e < 8; ++e) acc[h][c][e] = 0.f;
@@ -464,12 +403,6 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
         m[h] = -INFINITY;
         l[h] = 0.f;
       }
-#pragma unroll
-      for (int q = 0; q < GP; ++q) {
-        mo[q] = -INFINITY;
-        lo[q] = 0.f;
-      }
-      if constexpr (kQS) __syncwarp();
     }
 
     const uint16_t* Ks = reinterpret_cast<const uint16_t*>(ringK + (size_t)s * stage_half_bytes<D>());
@@ -478,7 +411,6 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
     // Scores of this warp's 2 x 4 tokens for its G query heads.
     float sc[2][G];
     bool valid[2];
-    const int hb = (li >> 2) & 1;  // paired heads: this lane keeps head 2q + hb
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
       const int tl = (p * NS + sub) * 4 + tg;
@@ -494,19 +426,9 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
           const uint32_t w[4] = {kv[c].x, kv[c].y, kv[c].z, kv[c].w};
-          float qv[8];
-          if constexpr (kQS) {
-            const float4* q4 = reinterpret_cast<const float4*>(qs + h * D + (c * 8 + li) * 8);
-            const float4 a0 = q4[0], a1 = q4[1];
-            qv[0] = a0.x; qv[1] = a0.y; qv[2] = a0.z; qv[3] = a0.w;
-            qv[4] = a1.x; qv[5] = a1.y; qv[6] = a1.z; qv[7] = a1.w;
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) qv[e] = qf[kQS ? 0 : h][c][e];
-          }
 #pragma unroll
           for (int e = 0; e < 4; ++e) {  // packed fp32x2 FMA: elements 2e, 2e+1
-            const float2 r = __ffma2_rn(make_float2(qv[2 * e], qv[2 * e + 1]),
+            const float2 r = __ffma2_rn(make_float2(qf[h][c][2 * e], qf[h][c][2 * e + 1]),
                                         make_float2(bf16lo(w[e]), bf16hi(w[e])),
                                         make_float2(acc0, acc1));
             acc0 = r.x;
@@ -515,64 +437,18 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
         }
         xs[h] = acc0 + acc1;
       }
-      if constexpr (kPair) {
 #pragma unroll
-        for (int q = 0; q < GP; ++q) {
-          float keep = hb ? xs[2 * q + 1] : xs[2 * q];
-          const float send = hb ? xs[2 * q] : xs[2 * q + 1];
-          keep += __shfl_xor_sync(0xffffffffu, send, 4);
-          keep += __shfl_xor_sync(0xffffffffu, keep, 2);
-          keep += __shfl_xor_sync(0xffffffffu, keep, 1);
-          sc[p][q] = valid[p] ? keep : -INFINITY;
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          float x = xs[h];
-          x += __shfl_xor_sync(0xffffffffu, x, 1);
-          x += __shfl_xor_sync(0xffffffffu, x, 2);
-          x += __shfl_xor_sync(0xffffffffu, x, 4);
-          sc[p][h] = valid[p] ? x : -INFINITY;
-        }
+      for (int h = 0; h < G; ++h) {
+        float x = xs[h];
+        x += __shfl_xor_sync(0xffffffffu, x, 1);
+        x += __shfl_xor_sync(0xffffffffu, x, 2);
+        x += __shfl_xor_sync(0xffffffffu, x, 4);
+        sc[p][h] = valid[p] ? x : -INFINITY;
       }
     }
 
     // Online softmax: one max update per stage (warp-uniform per head).
     float pr[2][G];
-    if constexpr (kPair) {
-#pragma unroll
-      for (int q = 0; q < GP; ++q) {
-        float mx = fmaxf(sc[0][q], sc[1][q]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        float alpha = 1.f;
-        if (mx > mo[q]) {
-          alpha = fast_exp2(mo[q] - mx);  // exp2(-inf) = 0 on the first stage
-          mo[q] = mx;
-          lo[q] *= alpha;
-        }
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-          const float ao = __shfl_xor_sync(0xffffffffu, alpha, 4);
-          const float a0 = hb ? ao : alpha, a1 = hb ? alpha : ao;
-#pragma unroll
-          for (int c = 0; c < NCH; ++c)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              acc[2 * q][c][e] *= a0;
-              acc[2 * q + 1][c][e] *= a1;
-            }
-        }
-        const float mu = mo[q] == -INFINITY ? 0.f : mo[q];
-        const float p0 = fast_exp2(sc[0][q] - mu), p1 = fast_exp2(sc[1][q] - mu);
-        lo[q] += p0 + p1;
-        const float o0 = __shfl_xor_sync(0xffffffffu, p0, 4);
-        const float o1 = __shfl_xor_sync(0xffffffffu, p1, 4);
-        pr[0][2 * q] = hb ? o0 : p0;
-        pr[0][2 * q + 1] = hb ? p0 : o0;
-        pr[1][2 * q] = hb ? o1 : p1;
-        pr[1][2 * q + 1] = hb ? p1 : o1;
-      }
-    } else {
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         float mx = fmaxf(sc[0][h], sc[1][h]);
@@ -591,7 +467,6 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
         pr[0][h] = fast_exp2(sc[0][h] - mu);
         pr[1][h] = fast_exp2(sc[1][h] - mu);
         l[h] += pr[0][h] + pr[1][h];
-      }
     }
 
     // acc += p * v
@@ -627,18 +502,6 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
     if (!(md.flags & F_LAST)) continue;
 
     // ---- end of this CTA's segment of sequence b: reduce over the 4 token groups
-    if constexpr (kPair) {  // both heads of each pair in every lane again
-      const int hb = (li >> 2) & 1;
-#pragma unroll
-      for (int q = 0; q < GP; ++q) {
-        const float mx = __shfl_xor_sync(0xffffffffu, mo[q], 4);
-        const float lx = __shfl_xor_sync(0xffffffffu, lo[q], 4);
-        m[2 * q] = hb ? mx : mo[q];
-        m[2 * q + 1] = hb ? mo[q] : mx;
-        l[2 * q] = hb ? lx : lo[q];
-        l[2 * q + 1] = hb ? lo[q] : lx;
-      }
-    }
 #pragma unroll
     for (int h = 0; h < G; ++h) {
       l[h] += __shfl_xor_sync(0xffffffffu, l[h], 8);
@@ -659,7 +522,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
       // the buffer through xfree[g] before the next segment's hand-off.
       writer = sub == 0;
       if (!writer) {
-        if (seg > 0 && !mbar_wait(&xfree[xi], (uint32_t)((seg - 1) & 1), a.status)) return;
+        if (seg > 0 && !mbar_wait(&xfree[g], (uint32_t)((seg - 1) & 1), a.status)) return;
         float* mine = xw + (size_t)warp * G * (D + 2);
         if (tg == 0) {
 #pragma unroll
@@ -675,14 +538,14 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&xfull[xi]);
+        if (lane == 0) mbar_arrive(&xfull[g]);
       } else {
-        if (!mbar_wait(&xfull[xi], (uint32_t)(seg & 1), a.status)) return;
+        if (!mbar_wait(&xfull[g], (uint32_t)(seg & 1), a.status)) return;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
           float M = m[h];
           for (int k = 1; k < NS; ++k)
-            M = fmaxf(M, xw[(size_t)((g + k * Hkv) * HS + hs) * G * (D + 2) + h * (D + 2) + D]);
+            M = fmaxf(M, xw[(size_t)(g + k * Hkv) * G * (D + 2) + h * (D + 2) + D]);
           const float Mu = M == -INFINITY ? 0.f : M;
           const float w0 = fast_exp2(m[h] - Mu);
           float ls = w0 * l[h];
@@ -691,7 +554,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[h][c][e] *= w0;
           for (int k = 1; k < NS; ++k) {
-            const float* o = xw + (size_t)((g + k * Hkv) * HS + hs) * G * (D + 2) + h * (D + 2);
+            const float* o = xw + (size_t)(g + k * Hkv) * G * (D + 2) + h * (D + 2);
             const float w = fast_exp2(o[D] - Mu);
             ls += w * o[D + 1];
 #pragma unroll
@@ -703,7 +566,7 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
           l[h] = ls;
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&xfree[xi]);
+        if (lane == 0) mbar_arrive(&xfree[g]);
       }
     }
     ++seg;
@@ -745,10 +608,12 @@ __device__ void decode_consumer(const DecodeArgs& a, const uint8_t* ringK, const
   }
 }
 
-template <int D, int G, int HS>
-__global__ void __maxnreg__(HS == 1 ? 168 : kSplitLaunchRegs) decode_split_kernel(const DecodeArgs a,
-                                                                const AppendArgs app) {
-  constexpr int CW = consumer_warps<HS>(), GE = G / HS, RS = ring_stages<D, G>();
+// The CUDA-core split kernel: 8 consumer warps + 1 producer warp.
+template <int D, int G>
+__global__ void __launch_bounds__((kBaseWarps + 1) * 32, 1)
+    decode_split_kernel(const DecodeArgs a, const AppendArgs app) {
+  static_assert(G <= 2, "groups of 4 and 8 query heads take the tensor-core kernel");
+  constexpr int RS = kStages;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* ringK = smem;
   uint8_t* ringV = smem + RS * stage_half_bytes<D>();
@@ -756,19 +621,18 @@ __global__ void __maxnreg__(HS == 1 ? 168 : kSplitLaunchRegs) decode_split_kerne
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + RS);
   uint64_t* empty = full + RS;
   uint64_t* xfull = empty + RS;
-  uint64_t* xfree = xfull + CW;
-  float* xw = reinterpret_cast<float*>(xfree + CW);
-  float* qs = xw + (size_t)CW * GE * (D + 2);
+  uint64_t* xfree = xfull + kBaseWarps;
+  float* xw = reinterpret_cast<float*>(xfree + kBaseWarps);
 
   if (threadIdx.x == 0) {
     // The merge kernel may be scheduled now; it waits for this grid to finish.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int i = 0; i < RS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], CW);
+      mbar_init(&empty[i], kBaseWarps);
     }
     const int ns = kBaseWarps / a.num_kv_heads;
-    for (int i = 0; i < CW; ++i) {
+    for (int i = 0; i < kBaseWarps; ++i) {
       mbar_init(&xfull[i], ns > 1 ? ns - 1 : 1);
       mbar_init(&xfree[i], 1);
     }
@@ -776,21 +640,10 @@ __global__ void __maxnreg__(HS == 1 ? 168 : kSplitLaunchRegs) decode_split_kerne
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5;
-  if constexpr (HS == 1) {
-    if (warp == CW)
-      decode_producer<D, RS, false>(a, app, nullptr, nullptr, ringK, ringV, meta, full, empty);
-    else
-      decode_consumer<D, GE, HS, RS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
-  } else {
-    if (warp >= CW) {
-      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSplitProducerRegs));
-      if (warp == CW)
-        decode_producer<D, RS, false>(a, app, nullptr, nullptr, ringK, ringV, meta, full, empty);
-    } else {
-      asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSplitConsumerRegs));
-      decode_consumer<D, GE, HS, RS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw, qs);
-    }
-  }
+  if (warp == kBaseWarps)
+    decode_producer<D, RS, false>(a, app, nullptr, nullptr, ringK, ringV, meta, full, empty);
+  else
+    decode_consumer<D, G, RS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw);
 }
 
 // ---------------------------------------------------------------- tensor-core consumers
@@ -1208,12 +1061,11 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const float* __restrict
 template <int D, int G>
 cudaError_t launch_decode_t(const DecodeArgs& a, const AppendArgs& app, int ctas,
                             cudaStream_t stream) {
-  constexpr int HS = head_split<D, G>();
-  const size_t smem = decode_smem_bytes<D, G>(ring_stages<D, G>());
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G, HS>,
+  const size_t smem = decode_smem_bytes<D, G>(kStages);
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_split_kernel<D, G, HS><<<ctas, block_warps<HS>() * 32, smem, stream>>>(a, app);
+  decode_split_kernel<D, G><<<ctas, (kBaseWarps + 1) * 32, smem, stream>>>(a, app);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -1303,9 +1155,10 @@ cudaError_t launch_decode_mma_t(DecodeArgs a, const AppendArgs& app, int ctas, c
   return launch_merge(a, D, ctas, stream);
 }
 
-// The tensor-core consumers serve every group size with the same instruction
-// count per token; the CUDA-core consumers stay for groups of one and two
-// query heads, where they stream at the HBM rate.
+// The tensor-core consumers serve groups of 4 and 8 query heads, where the
+// CUDA-core consumers are issue-bound (2 FMAs per K/V byte at G = 4); at one
+// or two heads per kv head the CUDA-core consumers stream at the HBM rate and
+// measured faster (decode B64 at 16/8/128: 97.4 against 99.7 us per call).
 template <int D, int G>
 constexpr bool use_mma() {
   return G >= 4;

@@ -77,7 +77,83 @@ __global__ void __launch_bounds__(kStoreThreads) kv_store_kernel(
   }
 }
 
+// The store of attn_prefill_varlen_append: few CTAs of 1024 threads (one per
+// SM, on half of the SMs at most), so that the prefill launched as its
+// programmatic dependent starts at once on the other SMs.  A warp copies two
+// rows at a time with all their 16-byte loads in flight before the stores;
+// the loads do not wait for the slots.
+constexpr int kNarrowThreads = 1024;
+
+__global__ void __launch_bounds__(kNarrowThreads, 1) kv_store_narrow_kernel(
+    const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, int64_t stride,
+    const int32_t* __restrict__ slots, int64_t n, uint16_t* __restrict__ k_cache,
+    uint16_t* __restrict__ v_cache, int64_t total_slots, int row_elems, int* status) {
+  // Launched as a programmatic dependent of the previous grid on the stream
+  // (which may have written k / v or still read the cache): wait for it to
+  // complete before touching memory; only the launch latency is overlapped.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int lane = threadIdx.x & 31;
+  const int nvec = row_elems >> 3;
+  const int64_t warps = (int64_t)gridDim.x * (kNarrowThreads / 32);
+  // Row pairs: pair p is token p (K row and V row).
+  for (int64_t t = (int64_t)blockIdx.x * (kNarrowThreads / 32) + (threadIdx.x >> 5); t < n;
+       t += warps) {
+    const int64_t s = slots[t];
+    const uint4* ks = reinterpret_cast<const uint4*>(k + t * stride);
+    const uint4* vs = reinterpret_cast<const uint4*>(v + t * stride);
+    for (int j0 = 0; j0 < nvec; j0 += 128) {
+      uint4 xk[4], xv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = j0 + 32 * j + lane;
+        if (i < nvec) {
+          xk[j] = ld_stream(ks + i);
+          xv[j] = ld_stream(vs + i);
+        }
+      }
+      if (s < 0) break;  // padding slot: nothing to write
+      if (s >= total_slots) {
+        if (lane == 0) record_error(status, KVP_ERR_DEVICE_DATA);
+        break;
+      }
+      uint4* kd = reinterpret_cast<uint4*>(k_cache + s * (int64_t)row_elems);
+      uint4* vd = reinterpret_cast<uint4*>(v_cache + s * (int64_t)row_elems);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int i = j0 + 32 * j + lane;
+        if (i < nvec) {
+          kd[i] = xk[j];
+          vd[i] = xv[j];
+        }
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_kv_store_narrow(const uint16_t* k, const uint16_t* v, int64_t stride,
+                                   const int32_t* slots, int64_t n, uint16_t* k_cache,
+                                   uint16_t* v_cache, int64_t total_slots, int row_elems,
+                                   int num_sms, int* status, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;
+  int64_t grid = (n + kNarrowThreads / 32 - 1) / (kNarrowThreads / 32);
+  const int64_t cap = num_sms / 2 > 0 ? num_sms / 2 : 1;
+  if (grid > cap) grid = cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kNarrowThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kv_store_narrow_kernel, k, v, stride, slots, n, k_cache, v_cache,
+                            total_slots, row_elems, status);
+}
 
 cudaError_t launch_kv_store(const uint16_t* k, const uint16_t* v, int64_t k_stride,
                             int64_t v_stride, const int32_t* slots, int64_t n, uint16_t* k_cache,

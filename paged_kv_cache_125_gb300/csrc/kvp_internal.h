@@ -31,6 +31,13 @@ cudaError_t launch_kv_store(const uint16_t* k, const uint16_t* v, int64_t k_stri
                             int64_t v_stride, const int32_t* slots, int64_t n, uint16_t* k_cache,
                             uint16_t* v_cache, int64_t total_slots, int row_elems, bool vec16,
                             int num_sms, int* status, cudaStream_t stream);
+// The store of attn_prefill_varlen_append (16-byte aligned rows; k and v
+// share a row stride): at most num_sms / 2 CTAs of 1024 threads, which let
+// the prefill launched as their programmatic dependent start on the others.
+cudaError_t launch_kv_store_narrow(const uint16_t* k, const uint16_t* v, int64_t stride,
+                                   const int32_t* slots, int64_t n, uint16_t* k_cache,
+                                   uint16_t* v_cache, int64_t total_slots, int row_elems,
+                                   int num_sms, int* status, cudaStream_t stream);
 
 // copy_blocks.cu
 cudaError_t launch_copy_blocks(uint16_t* cache, int64_t num_planes, int64_t plane_stride,
@@ -69,15 +76,14 @@ cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k
 // null if the driver does not provide it.
 void* tensor_map_encoder();
 bool prefill_supported(int num_heads, int num_kv_heads, int head_dim, int block_size);
-// New rows of a fused store (attn_prefill_varlen_append): row t of k / v
-// (row stride `stride`) goes to slot slot_mapping[t] of the caches.
+// New rows of attn_prefill_varlen_append, stored by a kv_store launch just
+// before the prefill: row t of k / v (row stride `stride`) is the key /
+// value of query row t.  The prefill is launched as a programmatic dependent
+// of the store and reads uncached keys from these rows.
 struct PrefillAppend {
   const uint16_t* k;
   const uint16_t* v;
   int64_t stride;
-  const int32_t* slot_mapping;
-  uint16_t* k_cache;
-  uint16_t* v_cache;
 };
 int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const uint16_t* k,
                    const uint16_t* v, int64_t kv_stride, int64_t total_k,

@@ -98,25 +98,17 @@ struct PrefillArgs {
   uint16_t* out;
   int64_t out_stride;
   int* status;
-  // Fused store (attn_prefill_varlen_append): row t of st_k / st_v goes to
-  // slot st_slots[t] of the caches.  append 1: paged keys, the rows are
-  // stored before any K/V load (grid-wide arrival counter st_ctr); append 2:
-  // packed keys (the new rows themselves), the store needs no ordering.
+  // attn_prefill_varlen_append: the grid is a programmatic dependent of the
+  // kv_store launch of the step's new rows.  append 1 (paged): uncached keys
+  // come from the new rows (maps tmKn / tmVn), and the first read of the cache
+  // waits for the store grid (griddepcontrol.wait); append 2 (packed): the
+  // keys are the new rows and nothing waits until the end.
   int append;
-  int row_elems;                 // num_kv_heads * D
-  const uint16_t* st_k;
-  const uint16_t* st_v;
-  int64_t st_stride;
-  const int32_t* st_slots;
-  int64_t st_rows;               // new rows (= total_q)
-  uint16_t* k_cache_w;
-  uint16_t* v_cache_w;
-  int64_t total_slots;
-  unsigned long long* st_ctr;    // (epoch << 32) | CTAs whose rows are stored
 };
 
 struct Item {
   int b, g, q0, q_len, cached, k_len, n_tiles;
+  int first;           // kv tile processed first; tile (first + j) % n_tiles is step j
   int rows_a, rows_b;  // valid tokens in tile A / B (rows_b may be 0)
   int q_row0;          // packed row of tile A's first token
   int k_row0;          // packed row of the sequence's first key (packed mode)
@@ -218,7 +210,17 @@ __device__ __forceinline__ bool decode_item(const PrefillArgs& a, const Cu& cu, 
   it.n_tiles = (kv_end + kBN - 1) / kBN;
   it.q_row0 = cq0 + it.q0;
   it.k_row0 = ck0;
+  // Fused store: tiles that read the cache (keys below `cached`) wait for the
+  // launch's store, so the item takes its uncached tiles first (the online
+  // softmax does not depend on the order of the kv tiles).
+  const int cache_tiles = a.append == 1 ? (it.cached + kBN - 1) / kBN : 0;
+  it.first = cache_tiles < it.n_tiles ? cache_tiles : 0;
   return true;
+}
+
+__device__ __forceinline__ int tile_at(const Item& it, int j) {
+  const int t = it.first + j;
+  return t < it.n_tiles ? t : t - it.n_tiles;
 }
 
 __device__ __forceinline__ int total_items(const PrefillArgs& a) {
@@ -395,105 +397,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// ------------------------------------------------------------------ fused store
-
-__device__ __forceinline__ uint4 ld_stream16(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
-// This CTA's share of the fused store: rows [r0, r1) of the 2 x st_rows
-// (token, K-or-V) rows, each row_elems bf16 (row_elems / 8 16-byte vectors).
-// A warp copies kRows rows at a time: it first issues every slot load and
-// every 16-byte data load of those rows (a lane holds 4 vectors of each row
-// per pass over 128 vectors), then the stores, so 4 * kRows loads per lane
-// are in flight and none waits for a slot.  A negative slot stores nothing
-// (padding); a slot past the pool is reported.
-template <int kRows>
-__device__ void store_rows(const PrefillArgs& a, int warp, int nwarps, int lane) {
-  const int64_t rows = 2 * a.st_rows;
-  const int64_t r0 = rows * blockIdx.x / gridDim.x, r1 = rows * (blockIdx.x + 1) / gridDim.x;
-  const int nvec = a.row_elems >> 3;
-  for (int64_t r = r0 + (int64_t)warp * kRows; r < r1; r += (int64_t)nwarps * kRows) {
-    int64_t slot[kRows];
-    const uint4* src[kRows];
-#pragma unroll
-    for (int k = 0; k < kRows; ++k) {
-      const int64_t rr = r + k;
-      const int64_t t = rr >> 1;
-      slot[k] = rr < r1 ? (int64_t)a.st_slots[t] : -1;
-      src[k] = reinterpret_cast<const uint4*>(((rr & 1) ? a.st_v : a.st_k) + t * a.st_stride);
-    }
-    for (int jb = 0; jb < nvec; jb += 128) {
-      uint4 val[kRows][4];
-#pragma unroll
-      for (int k = 0; k < kRows; ++k)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = jb + jj * 32 + lane;
-          if (r + k < r1 && j < nvec) val[k][jj] = ld_stream16(src[k] + j);
-        }
-#pragma unroll
-      for (int k = 0; k < kRows; ++k) {
-        if (slot[k] < 0) continue;
-        if (slot[k] >= a.total_slots) {
-          if (lane == 0 && jb == 0) record_error(a.status, KVP_ERR_DEVICE_DATA);
-          continue;
-        }
-        const int64_t rr = r + k;
-        uint4* dst = reinterpret_cast<uint4*>(((rr & 1) ? a.v_cache_w : a.k_cache_w) +
-                                              slot[k] * (int64_t)a.row_elems);
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const int j = jb + jj * 32 + lane;
-          if (j < nvec) dst[j] = val[k][jj];
-        }
-      }
-    }
-  }
-}
-
-// One arrival of this CTA on the launch's store counter: (epoch << 32) |
-// arrivals.  A value still tagged with another epoch (zero after the last
-// launch on this slot reset it) is moved to this epoch first, as in
-// queue_fetch; an arrival that landed on the stale value is made again.
-__device__ __forceinline__ void store_arrive(const PrefillArgs& a) {
-  const unsigned long long v = atomicAdd(a.st_ctr, 1ull);
-  if ((uint32_t)(v >> 32) == a.epoch) return;
-  const unsigned long long fresh = (unsigned long long)a.epoch << 32;
-  unsigned long long cur = v + 1ull;
-  for (int tries = 0; (uint32_t)(cur >> 32) != a.epoch; ++tries) {
-    if (tries > 4096) {
-      record_error(a.status, KVP_ERR_DEVICE_TIMEOUT);
-      return;
-    }
-    const unsigned long long prev = atomicCAS(a.st_ctr, cur, fresh);
-    cur = prev == cur ? fresh : prev;
-  }
-  atomicAdd(a.st_ctr, 1ull);
-}
-
-// Waits (one thread, bounded) until every CTA of the launch has stored its
-// rows; then the stores are visible to this CTA's tensor copies.
-__device__ bool store_wait(const PrefillArgs& a) {
-  const unsigned long long t0 = globaltimer_ns();
-  while (true) {
-    unsigned long long v;
-    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a.st_ctr) : "memory");
-    if ((uint32_t)(v >> 32) == a.epoch && (uint32_t)v >= gridDim.x) break;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      record_error(a.status, KVP_ERR_DEVICE_TIMEOUT);
-      return false;
-    }
-    __nanosleep(64);
-  }
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-  return true;
-}
-
 // ------------------------------------------------------------------ producer
 
 template <int D>
@@ -570,7 +473,7 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
     for (int j = 0; j < it.n_tiles; ++j, ++jt) {
       const int st = jt & 1;
       const uint32_t par = (jt >> 1) & 1;
-      const int key0 = j * kBN;
+      const int key0 = tile_at(it, j) * kBN;
       int nsub, rows_per_box;
       if (a.paged) {
         rows_per_box = a.sub_rows;
@@ -613,10 +516,12 @@ __device__ void producer_role(const PrefillArgs& a, const CUtensorMap* tmQ, cons
         rowi[0] = it.k_row0 + key0;
       }
       if (reads_cache && a.append == 1 && !stored) {
-        // A cache read: every CTA's share of the fused store must have landed.
-        int ok = 1;
-        if (lane == 0) ok = store_wait(a) ? 1 : 0;
-        if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+        // A cache read: the store grid of the step's new rows must be complete.
+        if (lane == 0) {
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
+        __syncwarp();
         stored = true;
       }
       for (int kv = 0; kv < 2; ++kv) {
@@ -750,7 +655,7 @@ __device__ void vfix_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars, c
     for (int j = 0; j < it.n_tiles; ++j, ++jt) {
       const int st = jt & 1;
       if (!mbar_wait(&bars[B_VFULL + st], (jt >> 1) & 1, a.status)) return;
-      const int valid_rows = it.k_len - j * kBN;
+      const int valid_rows = it.k_len - tile_at(it, j) * kBN;
       if (a.paged && valid_rows < kBN) {
         uint8_t* vs = smem + Lay::kV + st * Lay::kKVBytes;
         const int r0 = valid_rows < 0 ? 0 : valid_rows;
@@ -816,7 +721,7 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
       for (int c = 0; c < kBN / 32; ++c)
 #pragma unroll
         for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(sv[c][i]);
-      const int lim = pos - j * kBN;  // columns <= lim are visible
+      const int lim = pos - tile_at(it, j) * kBN;  // columns <= lim are visible
       if (lim < kBN - 1) {
 #pragma unroll
         for (int i = 0; i < kBN; ++i)
@@ -833,13 +738,16 @@ __device__ void softmax_role(const PrefillArgs& a, uint8_t* smem, uint64_t* bars
       float alpha = 1.f;
       bool rescale = false;
       if (j == 0) {
-        m = mxs;  // key 0 is visible to every row: finite
+        // In kv order the first tile holds key 0, which every row sees; with
+        // the uncached tiles first a row may see none of them (m = -inf).
+        m = mxs;
       } else if (mxs > m + kRescaleThreshold) {
-        alpha = fast_exp2(m - mxs);
+        alpha = fast_exp2(m - mxs);  // 0 while m is -inf (O and l are still 0)
         m = mxs;
         rescale = true;
       }
-      const float2 negm = make_float2(-m, -m);
+      const float mu = m == -INFINITY ? 0.f : m;
+      const float2 negm = make_float2(-mu, -mu);
       uint32_t pk[kBN / 2];
       float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
@@ -944,9 +852,15 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
   using Lay = Layout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   if (smem_u32(smem_raw) & 1023u) {  // the 128-byte swizzle needs a 1 KiB aligned base
-    if (threadIdx.x == 0) record_error(a.status, KVP_ERR_DEVICE_DATA);
+    if (threadIdx.x == 0) {
+      record_error(a.status, KVP_ERR_DEVICE_DATA);
+      if (a.append) asm volatile("griddepcontrol.wait;" ::: "memory");
+    }
     return;
   }
+  // The next call's store grid (launched as a programmatic dependent, and
+  // waiting for this grid before it touches memory) may be scheduled now.
+  if (a.append && threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   uint8_t* smem = smem_raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Lay::kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Lay::kNumBars);
@@ -992,19 +906,6 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
       vfix_role<D>(a, smem, bars, sc);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
-    if (a.append) {
-      // The fused store, by the softmax warps while the control warps set up
-      // the first item (their first S needs a K tile that comes after it).
-      store_rows<4>(a, threadIdx.x >> 5, 8, threadIdx.x & 31);
-      if (a.append == 1) {
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        named_barrier_sync(1, 256);
-        if (threadIdx.x == 0) {
-          __threadfence();
-          store_arrive(a);
-        }
-      }
-    }
     softmax_role<D>(a, smem, bars, tbase, sc);
   }
 
@@ -1012,24 +913,25 @@ __global__ void __launch_bounds__(kThreadsPF, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) tmem_dealloc(tbase, 512);
-  if ((a.dynamic || a.append == 1) && threadIdx.x == 0) {
-    // Every fetch and store wait of this CTA is done.  The last CTA to get
-    // here returns the counter slot to zero, so the same launch parameters (a
-    // CUDA graph replay) start from position 0 again.
+  if (a.dynamic && threadIdx.x == 0) {
+    // Every fetch of this CTA is done.  The last CTA to get here returns the
+    // counter slot to zero, so the same launch parameters (a CUDA graph
+    // replay) start from position 0 again.
     __threadfence();
     if (atomicAdd(a.qdone, 1u) == gridDim.x - 1) {
       atomicExch(a.qslot, 0ull);
-      if (a.st_ctr) atomicExch(a.st_ctr, 0ull);
       atomicExch(a.qdone, 0u);
     }
   }
+  // A dependent of the store grid does not complete before it (so the stream
+  // order after this call holds for the store as well).
+  if (a.append && threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Counter slots of the dynamic schedule: one per prefill launch in flight
 // (launch n uses slot n % kQueueSlots with epoch n / kQueueSlots + 1).
 __device__ unsigned long long g_queue_slot[kQueueSlots];
 __device__ unsigned int g_queue_done[kQueueSlots];
-__device__ unsigned long long g_store_ctr[kQueueSlots];  // fused store: arrivals per launch
 
 // ------------------------------------------------------------------ host side
 
@@ -1038,14 +940,12 @@ __device__ unsigned long long g_store_ctr[kQueueSlots];  // fused store: arrival
 constexpr int kMaxQueueDevices = 64;
 unsigned long long* g_qslot_ptr[kMaxQueueDevices];
 unsigned int* g_qdone_ptr[kMaxQueueDevices];
-unsigned long long* g_stctr_ptr[kMaxQueueDevices];
 std::atomic<unsigned long long> g_qseq[kMaxQueueDevices];
 std::mutex g_queue_mutex;
 
 struct QueueSlot {
-  unsigned long long* next;   // dynamic schedule counter
-  unsigned int* done;         // CTAs finished
-  unsigned long long* store;  // fused store arrivals
+  unsigned long long* next;  // dynamic schedule counter
+  unsigned int* done;        // CTAs finished
   uint32_t epoch;
 };
 
@@ -1057,20 +957,16 @@ bool queue_slot(QueueSlot* q) {
     if (!g_qslot_ptr[dev]) {
       void* ps = nullptr;
       void* pd = nullptr;
-      void* pc = nullptr;
       if (cudaGetSymbolAddress(&ps, g_queue_slot) != cudaSuccess ||
-          cudaGetSymbolAddress(&pd, g_queue_done) != cudaSuccess ||
-          cudaGetSymbolAddress(&pc, g_store_ctr) != cudaSuccess)
+          cudaGetSymbolAddress(&pd, g_queue_done) != cudaSuccess)
         return false;
       g_qdone_ptr[dev] = static_cast<unsigned int*>(pd);
-      g_stctr_ptr[dev] = static_cast<unsigned long long*>(pc);
       g_qslot_ptr[dev] = static_cast<unsigned long long*>(ps);
     }
   }
   const unsigned long long seq = g_qseq[dev].fetch_add(1);
   q->next = g_qslot_ptr[dev] + seq % kQueueSlots;
   q->done = g_qdone_ptr[dev] + seq % kQueueSlots;
-  q->store = g_stctr_ptr[dev] + seq % kQueueSlots;
   q->epoch = (uint32_t)(seq / kQueueSlots) + 1u;
   return true;
 }
@@ -1104,9 +1000,9 @@ bool make_map(CUtensorMap* m, const void* base, int64_t rows, int heads, int D, 
          CUDA_SUCCESS;
 }
 
-// A launch whose CTAs wait for each other (the fused store before paged
-// loads) is cooperative: it fails to launch instead of running with CTAs that
-// cannot all be resident (one CTA per SM, grid <= SMs).
+// attn_prefill_varlen_append launches the prefill as a programmatic
+// dependent of the store grid: its CTAs start on the SMs the (narrow) store
+// grid leaves free.
 template <int D>
 cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
                      const CUtensorMap& kn, const CUtensorMap& vn, const PrefillArgs& a, int grid,
@@ -1115,7 +1011,7 @@ cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)Layout<D>::kAlloc);
   if (e != cudaSuccess) return e;
-  if (a.append != 1) {
+  if (!a.append) {
     prefill_kernel<D><<<grid, kThreadsPF, Layout<D>::kAlloc, stream>>>(q, k, v, kn, vn, a);
     return cudaGetLastError();
   }
@@ -1125,8 +1021,8 @@ cudaError_t launch_t(const CUtensorMap& q, const CUtensorMap& k, const CUtensorM
   cfg.dynamicSmemBytes = Layout<D>::kAlloc;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, prefill_kernel<D>, q, k, v, kn, vn, a);
@@ -1215,35 +1111,15 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
   a.qslot = nullptr;
   a.qdone = nullptr;
   a.epoch = 0;
-  a.append = 0;
-  a.row_elems = num_kv_heads * head_dim;
-  a.st_k = a.st_v = nullptr;
-  a.st_stride = 0;
-  a.st_slots = nullptr;
-  a.st_rows = 0;
-  a.k_cache_w = a.v_cache_w = nullptr;
-  a.total_slots = 0;
-  a.st_ctr = nullptr;
-  if (app) {
-    a.append = paged ? 1 : 2;
-    a.st_k = app->k;
-    a.st_v = app->v;
-    a.st_stride = app->stride;
-    a.st_slots = app->slot_mapping;
-    a.st_rows = total_q;
-    a.k_cache_w = app->k_cache;
-    a.v_cache_w = app->v_cache;
-    a.total_slots = num_blocks * (int64_t)block_size;
-  }
-  if (a.dynamic || a.append == 1) {
+  a.append = app ? (paged ? 1 : 2) : 0;
+  if (a.dynamic) {
     QueueSlot qs;
     if (!queue_slot(&qs)) {
-      *why = "counter slots of the launch unavailable";
+      *why = "counter slots of the dynamic schedule unavailable";
       return KVP_ERR_CUDA;
     }
     a.qslot = qs.next;
     a.qdone = qs.done;
-    a.st_ctr = a.append == 1 ? qs.store : nullptr;
     a.epoch = qs.epoch;
   }
   a.cu_in_smem = num_seqs + 1 <= kCuCap ? 1 : 0;
