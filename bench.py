@@ -55,11 +55,18 @@ TRAFFIC = {
     "decode": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu",
                "sha256": "6714505f9679338af3c493ee75631c3e57932872a7e33bd5287ac720069b22d3",
                "bytes": 569288960 + 4451072},
-    # prefill workload (8 prompts, 32/8/128), one ncu --set full capture
+    # decode B512 mix: one capture of the tensor-core split kernel on 128 of the sequences
+    # (1790.12 MB for 1778.58 MB algorithmic), scaled to the 512-sequence launch by its algorithmic
+    # bytes (7062.70 MB)
+    "decode_b512": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu",
+                    "sha256": "ad1b2d380ba008f2599e85310180784f5339cf77cce8bec90c20afe4f31dda21",
+                    "bytes": 7108547269},
+    # prefill workload (8 prompts, 32/8/128), one ncu --set full capture of the prefill kernel of
+    # attn_prefill_varlen_append
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
-                "sha256": "7202843ebee04788acca15514bba8b861c474cba85d4a42595a64edce6a83eb4",
-                "bytes": 124059136 + 34817536},
-    # the prefill workload's suffix store (7.2k rows), one ncu capture
+                "sha256": "dee9572eec0f1aab8bcb4bc5fb5d62b841c14ca619dc101da703f29f6e14dcba",
+                "bytes": 111434496 + 33398272},
+    # the prefill workload's suffix store (8150 rows), one ncu capture
     "kv_store": {"file": "paged_kv_cache_125_gb300/csrc/kv_store.cu", "sha256": None, "bytes": None},
 }
 
@@ -362,9 +369,12 @@ def timed_loop_single(graphs, steps, warmup, world):
     return ms_step, statistics.mean(durs), (w0, w1)
 
 
-def timed_loop_eager(store_fn, attn_fn, sets, steps, warmup, world):
+def timed_loop_eager(store_fn, attn_fn, sets, steps, warmup, world, call_events=True):
     """As timed_loop, with the two calls launched directly (no graph): the
-    pages' engine runs prefill steps eagerly and graph-replays only decode."""
+    pages' engine runs prefill steps eagerly and graph-replays only decode.
+    Without call_events nothing is recorded between the steps (an event
+    record between two launches stops the second from starting early as a
+    programmatic dependent); the mean call time is then None."""
     import torch
     n = len(sets)
     for i in range(warmup):
@@ -378,16 +388,21 @@ def timed_loop_eager(store_fn, attn_fn, sets, steps, warmup, world):
     w0 = time.perf_counter()
     start.record()
     for i in range(steps):
-        evs[i][0].record()
+        if call_events:
+            evs[i][0].record()
         store_fn(sets[i % n])
-        evs[i][1].record()
+        if call_events:
+            evs[i][1].record()
         attn_fn(sets[i % n])
-        evs[i][2].record()
+        if call_events:
+            evs[i][2].record()
     stop.record()
     torch.cuda.synchronize()
     w1 = time.perf_counter()
     barrier(world)
     ms_step = start.elapsed_time(stop) / steps
+    if not call_events:
+        return ms_step, None, (w0, w1)
     durs = [b.elapsed_time(c) for a, b, c in evs]
     timed_loop_eager.last_store_ms = statistics.mean(a.elapsed_time(b) for a, b, c in evs)
     return ms_step, statistics.mean(durs), (w0, w1)
@@ -419,6 +434,14 @@ def oracle_decode_rate(w, min_seconds=8.0):
 
 
 # ----------------------------------------------------------------------------- main arms
+
+def bench_config(w, sets):
+    """The config dict both arms print: the workload and how the timed steps
+    avoid L2 reuse (input sets in rotation whose pools exceed the L2)."""
+    pools_gb = w.num_blocks * w.block_size * w.num_kv_heads * w.head_dim * 2 * 2 * sets / 1e9
+    return {"workload": w.description,
+            "l2": f"{sets} input sets in rotation ({pools_gb:.1f} GB of pools) vs 126 MB L2"}
+
 
 def run_reference(args, rank, world):
     """The oracle as it stands, timed on the host cores, on the same workload and
@@ -456,7 +479,8 @@ def run_reference(args, rank, world):
             "n_gpus": args.gpus, "steps": done, "warmup": warm,
             "ms_per_step": round(1000 * el / done, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.description, "parallelism": f"{cores} host threads"},
+            "config": bench_config(w, args.sets),
+            "parallelism": f"{cores} host threads",
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                              "sample": f"full decode step (store + decode of all 64 sequences) x {done}"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -549,7 +573,6 @@ def measure_decode(args, kvp, W, dev, stream, world, peaks):
                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                   "how": "packed pinned host inputs copied in (one copy), graph replay, output copied "
                          "out, stream sync each step"}
-    res["footprint_gb"] = sum(2 * s.kc.numel() * 2 for s in sets) / 1e9
     del app_graphs, sets, e2e_graph
     return res
 
@@ -565,8 +588,10 @@ def measure_prefill(args, kvp, W, dev, stream, world, peaks):
     flops = prefill_flops(wp)
     psets = [DeviceSet(wp, dev) for _ in range(args.sets)]
     psteps = args.prefill_steps or max(50, args.steps // 4)
-    ms_pstep, ms_fused, pwin = timed_loop_eager(no_call, lambda s_: prefill_append_call(kvp, s_, wp),
-                                                psets, psteps, args.warmup, world)
+    ms_pstep, _, pwin = timed_loop_eager(no_call, lambda s_: prefill_append_call(kvp, s_, wp),
+                                         psets, psteps, args.warmup, world, call_events=False)
+    _, ms_fused, _ = timed_loop_eager(no_call, lambda s_: prefill_append_call(kvp, s_, wp), psets,
+                                      psteps, args.warmup, world)
     assert kvp.device_status() == 0, "device status after the timed prefill loop"
     ms_step2, ms_prefill, pwin2 = timed_loop_eager(lambda s_: store_call(kvp, s_),
                                                    lambda s_: prefill_call(kvp, s_, wp), psets, psteps,
@@ -631,8 +656,10 @@ def measure_mixed(args, kvp, W, dev, stream, world, peaks):
     nbytes = kv_bytes + qo_bytes + st_bytes
     msets = [DeviceSet(wm, dev) for _ in range(2)]
     steps = max(50, min(400, args.steps // 10))
-    ms_step, ms_call, win = timed_loop_eager(no_call, lambda s_: prefill_append_call(kvp, s_, wm), msets,
-                                             steps, args.warmup, world)
+    ms_step, _, win = timed_loop_eager(no_call, lambda s_: prefill_append_call(kvp, s_, wm), msets,
+                                       steps, args.warmup, world, call_events=False)
+    _, ms_call, _ = timed_loop_eager(no_call, lambda s_: prefill_append_call(kvp, s_, wm), msets, steps,
+                                     args.warmup, world)
     assert kvp.device_status() == 0, "device status after the mixed loop"
     fps, ms_step = aggregate(flops, ms_step, world)
     tf_call = flops / (ms_call * 1e-3) / 1e12
@@ -766,7 +793,8 @@ def measure_decode_large(args, kvp, W, dev, stream, world, peaks):
                      "roofline": {"kernel": "attn_decode_paged_append (store + split + merge)",
                                   "bound": "hbm",
                                   "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                  "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                                  "frac": round(achieved / peaks["hbm_gbs"], 4),
+                                  "traffic": traffic_for("decode_b512") if args.b512_batch == 512 else None,
                                   "algorithmic_bytes": store_b + dec_b, "peak_source": peaks["source"],
                                   "ms_per_launch": round(ms_dec, 5)}}}
 
@@ -841,35 +869,40 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
             work = decode_bytes(st.meta, n, hq, hkv, d, bs)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
+        h0 = time.perf_counter()
         eng.launch(st, q, k, v)
+        host_us = (time.perf_counter() - h0) * 1e6
         b.record()
-        recs.append((st.is_prefill, work * layers, a, b, n, len(st.seq_ids)))
+        recs.append((st.is_prefill, work * layers, a, b, n, len(st.seq_ids), host_us))
         eng.commit(st, [(7 * i + n) % 151936 for i in st.seq_ids])
         del q, k, v
     torch.cuda.synchronize()
     w1 = time.perf_counter()
     assert kvp.device_status() == 0, "device status after the trace replay"
-    dec_ms = sum(a.elapsed_time(b) for p_, _, a, b, _, _ in recs if not p_)
-    pre_ms = sum(a.elapsed_time(b) for p_, _, a, b, _, _ in recs if p_)
+    dec_ms = sum(a.elapsed_time(b) for p_, _, a, b, *_ in recs if not p_)
+    pre_ms = sum(a.elapsed_time(b) for p_, _, a, b, *_ in recs if p_)
     dec_work = sum(w_ for p_, w_, *_ in recs if not p_)
     pre_work = sum(w_ for p_, w_, *_ in recs if p_)
     n_dec = sum(1 for r in recs if not r[0])
     # prefill steps by query tokens
     groups = {}
-    for p_, w_, a, b, n, ns in recs:
+    for p_, w_, a, b, n, ns, host_us in recs:
         if not p_:
             continue
         key = ">=8192 tokens" if n >= 8192 else ("1024-8191 tokens" if n >= 1024 else "<1024 tokens")
-        g = groups.setdefault(key, {"steps": 0, "tokens": 0, "seqs": 0, "ms": 0.0, "tflop": 0.0})
+        g = groups.setdefault(key, {"steps": 0, "tokens": 0, "seqs": 0, "ms": 0.0, "tflop": 0.0,
+                                    "host_ms": 0.0})
         g["steps"] += 1
         g["tokens"] += n
         g["seqs"] += ns
         g["ms"] += a.elapsed_time(b)
         g["tflop"] += w_ / 1e12
+        g["host_ms"] += host_us / 1e3
     for g in groups.values():
         g["ms"] = round(g["ms"], 3)
         g["tflop"] = round(g["tflop"], 4)
         g["us_per_layer_call"] = round(g["ms"] * 1e3 / (g["steps"] * layers), 2)
+        g["host_us_per_layer_call"] = round(g.pop("host_ms") * 1e3 / (g["steps"] * layers), 2)
         g["tflops"] = round(g["tflop"] / (g["ms"] * 1e-3), 1)
     preempt = eng.num_preemptions
     del eng
@@ -1061,18 +1094,18 @@ def run_ours(args, rank, world, local):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dec["ms_step"], 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.description,
-                       "step": "attn_decode_paged_append: kv_store of the 64 new rows fused into the "
-                               "paged decode (split + merge)",
-                       "global_batch": 64 * world, "parallelism": f"replicas x{world}",
-                       "l2": f"{args.sets} input sets in rotation ({dec['footprint_gb']:.1f} GB of pools) vs 126 MB L2",
-                       "graph": "each step is one CUDA graph replay"},
+            "config": bench_config(w, args.sets),
+            "setup": {"step": "attn_decode_paged_append: kv_store of the 64 new rows fused into the "
+                              "paged decode (split + merge)",
+                      "global_batch": 64 * world,
+                      "graph": "each step is one CUDA graph replay"},
+            "parallelism": f"replicas x{world}",
             "roofline": dec["roofline"], "cpu_baseline": cpu, "e2e": dec["e2e"],
             "unfused": dec["unfused"],
             "gpu_launches": 2 * args.steps + 3 * args.steps
-                            + (0 if pre is None else 3 * pre["line"]["steps"])
+                            + (0 if pre is None else 6 * pre["line"]["steps"])
                             + (0 if cb is None else cb["line"]["steps"])
-                            + (0 if mx is None else mx["steps"])
+                            + (0 if mx is None else 4 * mx["steps"])
                             + (0 if bk is None else 2 * bk["steps"])
                             + (0 if g8 is None else 2 * g8["steps"])
                             + (0 if dl is None else 2 * dl["steps"])
@@ -1083,12 +1116,15 @@ def run_ours(args, rank, world, local):
                                                           "decode_split": args.steps,
                                                           "decode_merge": args.steps},
                                        "prefill": None if pre is None else
-                                       {"prefill_append": pre["line"]["steps"],
+                                       {"kv_store_narrow (fused calls, 2 loops)": 2 * pre["line"]["steps"],
+                                        "prefill (fused calls, 2 loops)": 2 * pre["line"]["steps"],
                                         "kv_store (two-call loop)": pre["line"]["steps"],
                                         "prefill (two-call loop)": pre["line"]["steps"]},
                                        "copy_blocks": None if cb is None else
                                        {"kv_copy_blocks": cb["line"]["steps"]},
-                                       "mixed": None if mx is None else {"prefill_append": mx["steps"]},
+                                       "mixed": None if mx is None else
+                                       {"kv_store_narrow (2 loops)": 2 * mx["steps"],
+                                        "prefill (2 loops)": 2 * mx["steps"]},
                                        "engine_trace": None if tr is None else {"all": tr["launches"]},
                                        "decode_b512": None if dl is None or not dl["steps"] else
                                        {"decode_split": dl["steps"], "decode_merge": dl["steps"]},
