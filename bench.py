@@ -641,13 +641,20 @@ def measure_prefill(args, kvp, W, dev, stream, world, peaks):
 
 
 def measure_mixed(args, kvp, W, dev, stream, world, peaks):
-    """One engine step mixing chunked prefill and decode in a single varlen
-    paged prefill call (4 prompt chunks, 3772 tokens, + 128 decode rows,
-    32/8/128): attn_prefill_varlen_append (the store of the new rows fused
-    into the attention call), launched eagerly over 2 input sets in rotation."""
+    """One engine step mixing chunked prefill and decode (4 prompt chunks,
+    3772 tokens, + 128 decode rows, 32/8/128), launched eagerly over 2 input
+    sets in rotation.  The step is attn_mixed_step: the chunks through the
+    fused store + prefill on part of the SMs, the decode rows through the
+    decode kernel (store fused) on the others (7/12 of the SMs by default),
+    side by side; a short sweep of
+    the decode rows' SM share, and the same step as one
+    attn_prefill_varlen_append call (decode rows as q_len-1 sequences of the
+    prefill kernel), are reported beside it."""
+    import torch
     wm = W.mixed_step_workload()
     flops = prefill_flops(wm)
     m = wm.steps[0].attn.meta
+    nd = 128
     # algorithmic bytes: K and V of every sequence's keys once per kv head, q read, out written,
     # the new rows read and stored
     kv_bytes = int(m.cu_seqlens_k[-1]) * wm.num_kv_heads * wm.head_dim * 2 * 2
@@ -655,38 +662,47 @@ def measure_mixed(args, kvp, W, dev, stream, world, peaks):
     st_bytes = int(m.cu_seqlens_q[-1]) * (4 * wm.num_kv_heads * wm.head_dim * 2 + 4)
     nbytes = kv_bytes + qo_bytes + st_bytes
     msets = [DeviceSet(wm, dev) for _ in range(2)]
+    ws = torch.empty(kvp.attn_decode_workspace_size(nd, wm.num_heads, wm.head_dim, m.max_seqlen_k,
+                                                    wm.block_size), dtype=torch.uint8, device=dev)
     steps = max(50, min(400, args.steps // 10))
-    ms_step, _, win = timed_loop_eager(no_call, lambda s_: prefill_append_call(kvp, s_, wm), msets,
-                                       steps, args.warmup, world, call_events=False)
-    _, ms_call, _ = timed_loop_eager(no_call, lambda s_: prefill_append_call(kvp, s_, wm), msets, steps,
-                                     args.warmup, world)
-    assert kvp.device_status() == 0, "device status after the mixed loop"
+
+    def mixed(s_, dsms=0):
+        kvp.attn_mixed_step(s_.q, s_.k, s_.v, s_.slots, s_.cu_q, s_.cu_k, s_.max_q, s_.max_k, s_.kc, s_.vc,
+                            s_.bt, nd, decode_sms=dsms, softmax_scale=wm.scale, workspace=ws, out=s_.out)
+
+    ms_step, _, win = timed_loop_eager(no_call, mixed, msets, steps, args.warmup, world, call_events=False)
+    _, ms_call, _ = timed_loop_eager(no_call, mixed, msets, steps, args.warmup, world)
+    sweep = {}
+    for dsms in (64, 76, 100, 112):
+        t, _, _ = timed_loop_eager(no_call, lambda s_: mixed(s_, dsms), msets, steps, 3, world,
+                                   call_events=False)
+        sweep[str(dsms)] = round(nbytes / (t * 1e-3) / 1e9, 1)
+    ms_one, _, _ = timed_loop_eager(no_call, lambda s_: prefill_append_call(kvp, s_, wm), msets, steps,
+                                    args.warmup, world, call_events=False)
+    assert kvp.device_status() == 0, "device status after the mixed loops"
     fps, ms_step = aggregate(flops, ms_step, world)
     tf_call = flops / (ms_call * 1e-3) / 1e12
     gbs_call = nbytes / (ms_call * 1e-3) / 1e9
-    # the binding roofline is the larger of the two lower bounds on the call's time
-    hbm_bound = nbytes / (peaks["hbm_gbs"] * 1e9) >= flops / (peaks["bf16_tflops"] * 1e12)
-    del msets
+    del msets, ws
     return {"window": win, "steps": steps,
-            "line": {"workload": wm.description, "value": round(fps / 1e12, 2), "unit": "TFLOP/s",
-                     "ms_per_step": round(ms_step, 4), "steps": steps,
-                     "step": "attn_prefill_varlen_append over chunks and decode rows (store fused)",
-                     "roofline": ({"kernel": "attn_prefill_varlen_append (mixed)", "bound": "hbm",
-                                   "achieved": round(gbs_call, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                   "frac": round(gbs_call / peaks["hbm_gbs"], 4), "traffic": None,
-                                   "algorithmic_bytes": nbytes, "peak_source": peaks["source"],
-                                   "ms_per_launch": round(ms_call, 5),
-                                   "tensor": {"achieved_tflops": round(tf_call, 1),
-                                              "frac_of_bf16_burst": round(tf_call / peaks["bf16_tflops"], 4),
-                                              "algorithmic_flops": flops}}
-                                  if hbm_bound else
-                                  {"kernel": "attn_prefill_varlen_append (mixed)", "bound": "tensor",
-                                   "achieved": round(tf_call, 1), "peak": peaks["bf16_tflops"],
-                                   "unit": "TFLOP/s", "frac": round(tf_call / peaks["bf16_tflops"], 4),
-                                   "traffic": None, "algorithmic_flops": flops,
-                                   "peak_source": peaks["source"] + " bf16 burst",
-                                   "ms_per_launch": round(ms_call, 5),
-                                   "hbm": {"achieved_gbs": round(gbs_call, 1), "algorithmic_bytes": nbytes}})}}
+            "line": {"workload": wm.description, "value": round(nbytes / (ms_step * 1e-3) / 1e9, 1),
+                     "unit": "GB/s", "ms_per_step": round(ms_step, 4), "steps": steps,
+                     "step": "attn_mixed_step: chunks (store + prefill) beside the 128 decode rows "
+                             "(decode, store fused) on 88 of the 152 SMs, one stream, chained by programmatic "
+                             "dependent launches",
+                     "roofline": {"kernel": "attn_mixed_step (store + prefill | decode)", "bound": "hbm",
+                                  "achieved": round(gbs_call, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": round(gbs_call / peaks["hbm_gbs"], 4), "traffic": None,
+                                  "algorithmic_bytes": nbytes, "peak_source": peaks["source"],
+                                  "ms_per_launch": round(ms_call, 5),
+                                  "tensor": {"achieved_tflops": round(tf_call, 1),
+                                             "frac_of_bf16_burst": round(tf_call / peaks["bf16_tflops"], 4),
+                                             "algorithmic_flops": flops}},
+                     "decode_sms_sweep_gbs": sweep,
+                     "one_call": {"step": "attn_prefill_varlen_append over chunks and decode rows",
+                                  "ms_per_step": round(ms_one, 4),
+                                  "value": round(nbytes / (ms_one * 1e-3) / 1e9, 1), "unit": "GB/s",
+                                  "frac_of_hbm": round(nbytes / (ms_one * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)}}}
 
 
 def measure_bucketed(args, kvp, W, dev, stream, world, peaks):
@@ -842,7 +858,8 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
     the prefill steps (causal FLOPs), each timed by an event pair around
     ``launch`` (for decode: the copy of the step's packed metadata into the
     graph's buffer and the replay).  Prefill steps are also broken down by
-    their query tokens."""
+    their query tokens, with the host's issue time per layer call (measured
+    with an empty launch queue)."""
     import torch
     from paged_kv_cache_125_gb300 import engine_trace as E
     from paged_kv_cache_125_gb300.engine_replay import EngineReplay, decode_bytes, prefill_flops
@@ -868,6 +885,14 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
             v.copy_(torch.randn(v.shape, generator=gq, device=dev))
             work = decode_bytes(st.meta, n, hq, hkv, d, bs)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if st.is_prefill:
+            # Drain the launch queue (the host runs steps ahead of the device,
+            # and a full queue blocks launches), then keep the device busy for
+            # ~100 us outside the event pair while the host issues the layers:
+            # host_us is then the issue time alone, and the events see no
+            # start-up gap.
+            torch.cuda.synchronize()
+            torch.cuda._sleep(200_000)
         a.record()
         h0 = time.perf_counter()
         eng.launch(st, q, k, v)
@@ -920,7 +945,7 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
                                  "frac_of_bf16_burst": round(pre_tf / peaks["bf16_tflops"], 4),
                                  "by_query_tokens": groups},
                      "how": "EngineReplay: event pair around each step's launch of 28 layers (prefill: "
-                            "kv_store + attn_prefill_varlen per layer, eager; decode: one copy of the "
+                            "attn_prefill_varlen_append per layer, eager; decode: one copy of the "
                             "packed metadata from pinned memory + one 28-layer graph replay of "
                             "attn_decode_paged_append per bucket); per-layer inputs generated on the "
                             "device before each step"}}
@@ -1105,7 +1130,7 @@ def run_ours(args, rank, world, local):
             "gpu_launches": 2 * args.steps + 3 * args.steps
                             + (0 if pre is None else 6 * pre["line"]["steps"])
                             + (0 if cb is None else cb["line"]["steps"])
-                            + (0 if mx is None else 4 * mx["steps"])
+                            + (0 if mx is None else 26 * mx["steps"])
                             + (0 if bk is None else 2 * bk["steps"])
                             + (0 if g8 is None else 2 * g8["steps"])
                             + (0 if dl is None else 2 * dl["steps"])
@@ -1123,8 +1148,9 @@ def run_ours(args, rank, world, local):
                                        "copy_blocks": None if cb is None else
                                        {"kv_copy_blocks": cb["line"]["steps"]},
                                        "mixed": None if mx is None else
-                                       {"kv_store_narrow (2 loops)": 2 * mx["steps"],
-                                        "prefill (2 loops)": 2 * mx["steps"]},
+                                       {"attn_mixed_step: store, prefill, split, merge (6 loops)":
+                                        24 * mx["steps"],
+                                        "attn_prefill_varlen_append: store, prefill (1 loop)": 2 * mx["steps"]},
                                        "engine_trace": None if tr is None else {"all": tr["launches"]},
                                        "decode_b512": None if dl is None or not dl["steps"] else
                                        {"decode_split": dl["steps"], "decode_merge": dl["steps"]},

@@ -10,6 +10,7 @@
  *   attn_decode_paged    one query token per sequence over its paged history
  *   attn_decode_paged_append  kv_store of the new rows + attn_decode_paged, fused
  *   attn_prefill_varlen_append  kv_store of the new rows + attn_prefill_varlen, fused
+ *   attn_mixed_step      a step of prefill chunks and decode rows, the two side by side
  *
  * Sources: "nano-vLLM-1" (Senjl's Digital Garden), ModelRunner sections
  * "3. KV cache 分配", "4. prefill 输入打包", "5. deocde 输入打包" and BlockManager
@@ -231,6 +232,49 @@ int attn_prefill_varlen_append(const kvp_bf16 *q, int64_t q_stride_tok, int64_t 
                                int num_seqs, const int64_t *positions, int num_heads,
                                int num_kv_heads, int head_dim, float softmax_scale, kvp_bf16 *out,
                                int64_t out_stride_tok, kvp_stream_t stream);
+
+/*
+ * attn_mixed_step - one engine step that mixes chunked prefill and decode:
+ * kv_store of every new row, then attn_prefill_varlen (paged) over all
+ * sequences, where the last num_decode_seqs sequences are decode rows (one
+ * query row each, q_len 1; their query rows are the last num_decode_seqs rows).
+ *
+ * Source: the mixed step is the chunked-prefill extension that "nano-vLLM-1"
+ * names (the pages' engine runs prefill-only or decode-only steps); its
+ * decode rows follow "5. deocde 输入打包" (one token per sequence at position
+ * len - 1) and its chunks "4. prefill 输入打包" (a suffix whose cached prefix
+ * may end inside a block).
+ *
+ * Arguments as attn_prefill_varlen_append (block_tables required), plus:
+ *   num_decode_seqs  0 .. num_seqs: the trailing decode rows.  Each must have
+ *                    q_len 1 (otherwise KVP_ERR_DEVICE_DATA is recorded) and
+ *                    its slot_mapping entry must be the slot of its position
+ *                    k_len - 1 (as attn_decode_paged_append requires)
+ *   decode_sms       SMs given to the decode rows while the chunks run on the
+ *                    others (0 = 7/12 of the device's SMs, 88 of 152)
+ *   workspace        as attn_decode_paged, for the decode rows: at least
+ *                    attn_decode_workspace_size(num_decode_seqs, num_heads,
+ *                    head_dim, max_seqlen_k, block_size) bytes
+ * Everything is enqueued on the caller's stream as one chain of programmatic
+ * dependent launches: the store of the chunks' rows and the prefill of
+ * attn_prefill_varlen_append on device SMs - decode_sms SMs, then the decode
+ * (store fused) of attn_decode_paged_append on the other decode_sms SMs,
+ * which starts as soon as the prefill grid is resident and completes after
+ * it, then the decode's merge.  The chunks and the decode rows thus run side
+ * by side, and work enqueued on the stream after the call sees both done.
+ * The two halves read and write disjoint slots (a decode row writes its own
+ * last block; a chunk writes its own uncached blocks).  The call holds no
+ * stream or event of its own and may be captured in a CUDA graph.
+ */
+int attn_mixed_step(const kvp_bf16 *q, int64_t q_stride_tok, int64_t total_q, const kvp_bf16 *k,
+                    const kvp_bf16 *v, int64_t kv_stride_tok, const int32_t *slot_mapping,
+                    kvp_bf16 *k_cache, kvp_bf16 *v_cache, int64_t num_blocks, int block_size,
+                    const int32_t *block_tables, int max_blocks_per_seq,
+                    const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k, int max_seqlen_q,
+                    int max_seqlen_k, int num_seqs, int num_decode_seqs, int decode_sms,
+                    int num_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                    void *workspace, size_t workspace_bytes, kvp_bf16 *out,
+                    int64_t out_stride_tok, kvp_stream_t stream);
 
 /*
  * Bytes of device workspace attn_decode_paged needs for this shape on the

@@ -21,6 +21,7 @@ import os
 import threading
 
 __all__ = ["kv_store", "kv_copy_blocks", "attn_prefill_varlen", "attn_prefill_varlen_append",
+           "attn_mixed_step",
            "attn_decode_paged", "attn_decode_workspace_size", "attn_decode_paged_noalloc",
            "attn_decode_paged_append",
            "device_status", "selftest_wait", "library", "library_path", "KvpError"]
@@ -54,6 +55,9 @@ SIGNATURES = {
     "attn_prefill_varlen_append": (_I32, [_P, _I64, _I64, _P, _P, _I64, _P, _P, _P, _I64, _I32, _P, _I32,
                                           _P, _P, _I32, _I32, _I32, _P, _I32, _I32, _I32, _F32, _P, _I64,
                                           _P]),
+    "attn_mixed_step": (_I32, [_P, _I64, _I64, _P, _P, _I64, _P, _P, _P, _I64, _I32, _P, _I32, _P, _P,
+                               _I32, _I32, _I32, _I32, _I32, _I32, _I32, _I32, _F32, _P, _SZ, _P, _I64,
+                               _P]),
 }
 
 
@@ -387,4 +391,49 @@ def attn_prefill_varlen_append(q, k, v, slot_mapping, cu_seqlens_q, cu_seqlens_k
         _ptr(q), qs, tq, _ptr(k), _ptr(v), kvs, _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), nb,
         bs, _ptr(block_tables), mb, _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_seqlen_q),
         int(max_seqlen_k), nseq, _ptr(positions), hq, hkv, d, scale, _ptr(out), os_, _stream(q)))
+    return out
+
+
+def attn_mixed_step(q, k, v, slot_mapping, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                    max_seqlen_k: int, k_cache, v_cache, block_tables, num_decode_seqs: int,
+                    decode_sms: int = 0, softmax_scale: float | None = None, workspace=None, out=None):
+    """A step of prefill chunks and decode rows (the last num_decode_seqs
+    sequences, one query row each): kv_store of every new row, then the
+    paged varlen prefill over all sequences, with the decode rows run by the
+    decode kernel beside the chunks (see include/kvpaged.h)."""
+    import torch
+    nb, bs, hkv, d = _cache_dims(k_cache, v_cache)
+    dev = k_cache.device
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        _require(t, name, torch.bfloat16, 3, dev)
+    tq, hq = q.shape[0], q.shape[1]
+    qs = _rows(q, "q", hq, d)
+    kvs = _rows(k, "k", hkv, d)
+    if _rows(v, "v", hkv, d) != kvs:
+        raise ValueError("k and v must share a row stride")
+    _require(slot_mapping, "slot_mapping", torch.int32, 1, dev)
+    if k.shape[0] != tq or v.shape[0] != tq or slot_mapping.shape[0] != tq or \
+            not slot_mapping.is_contiguous():
+        raise ValueError("k, v and slot_mapping must have one (contiguous) row per query row")
+    _require(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1, dev)
+    _require(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1, dev)
+    nseq = cu_seqlens_q.shape[0] - 1
+    if cu_seqlens_k.shape[0] != nseq + 1:
+        raise ValueError("cu_seqlens_q / cu_seqlens_k lengths differ")
+    _require(block_tables, "block_tables", torch.int32, 2, dev)
+    if block_tables.shape[0] != nseq or not block_tables.is_contiguous():
+        raise ValueError("block_tables must be contiguous [num_seqs, max_blocks]")
+    if out is None:
+        out = torch.empty((tq, hq, d), dtype=torch.bfloat16, device=dev)
+    _require(out, "out", torch.bfloat16, 3, dev)
+    os_ = _rows(out, "out", hq, d)
+    need = attn_decode_workspace_size(max(num_decode_seqs, 1), hq, d, int(max_seqlen_k), bs)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    _check(library().attn_mixed_step(
+        _ptr(q), qs, tq, _ptr(k), _ptr(v), kvs, _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache), nb, bs,
+        _ptr(block_tables), block_tables.shape[1], _ptr(cu_seqlens_q), _ptr(cu_seqlens_k), int(max_seqlen_q),
+        int(max_seqlen_k), nseq, int(num_decode_seqs), int(decode_sms), hq, hkv, d, scale, _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(out), os_, _stream(q)))
     return out

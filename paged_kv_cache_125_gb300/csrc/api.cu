@@ -383,7 +383,7 @@ int attn_prefill_varlen_append(const kvp_bf16* q, int64_t q_stride_tok, int64_t 
   cudaError_t e = kvp::launch_kv_store_narrow(k, v, kv_stride_tok, slot_mapping, total_q, k_cache,
                                               v_cache, num_blocks * (int64_t)block_size,
                                               num_kv_heads * head_dim, sms, status,
-                                              (cudaStream_t)stream);
+                                              (cudaStream_t)stream, true);
   if (e != cudaSuccess) return fail_cuda(e, "attn_prefill_varlen_append store launch");
   const kvp::PrefillAppend app{k, v, kv_stride_tok};
   const char* why = nullptr;
@@ -393,6 +393,101 @@ int attn_prefill_varlen_append(const kvp_bf16* q, int64_t q_stride_tok, int64_t 
                            num_heads, num_kv_heads, head_dim, softmax_scale, out, out_stride_tok,
                            sms, status, (cudaStream_t)stream, &why, &app);
   if (rc) return fail(rc, "%s: %s", fn, why ? why : "launch failed");
+  return KVP_OK;
+}
+
+int attn_mixed_step(const kvp_bf16* q, int64_t q_stride_tok, int64_t total_q, const kvp_bf16* k,
+                    const kvp_bf16* v, int64_t kv_stride_tok, const int32_t* slot_mapping,
+                    kvp_bf16* k_cache, kvp_bf16* v_cache, int64_t num_blocks, int block_size,
+                    const int32_t* block_tables, int max_blocks_per_seq,
+                    const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int max_seqlen_q,
+                    int max_seqlen_k, int num_seqs, int num_decode_seqs, int decode_sms,
+                    int num_heads, int num_kv_heads, int head_dim, float softmax_scale,
+                    void* workspace, size_t workspace_bytes, kvp_bf16* out,
+                    int64_t out_stride_tok, kvp_stream_t stream) {
+  const char* fn = "attn_mixed_step";
+  if (num_seqs < 0 || num_decode_seqs < 0 || num_decode_seqs > num_seqs || decode_sms < 0 ||
+      max_seqlen_q < 0 || max_seqlen_k < 0 || total_q < 0 || total_q >= ((int64_t)1 << 31) ||
+      num_decode_seqs > total_q)
+    return fail(KVP_ERR_INVALID_ARG, "%s: bad sizes", fn);
+  if (!kvp::prefill_supported(num_heads, num_kv_heads, head_dim, block_size) ||
+      !kvp::decode_supported(num_heads, num_kv_heads, head_dim))
+    return fail(KVP_ERR_UNSUPPORTED, "%s: unsupported heads %d/%d, head_dim %d or block_size %d",
+                fn, num_heads, num_kv_heads, head_dim, block_size);
+  if (q_stride_tok < (int64_t)num_heads * head_dim || out_stride_tok < (int64_t)num_heads * head_dim ||
+      kv_stride_tok < (int64_t)num_kv_heads * head_dim)
+    return fail(KVP_ERR_INVALID_ARG, "%s: row stride too small", fn);
+  if (num_blocks <= 0 || max_blocks_per_seq <= 0)
+    return fail(KVP_ERR_INVALID_ARG, "%s: num_blocks and max_blocks_per_seq must be positive", fn);
+  if (num_blocks * (int64_t)block_size >= ((int64_t)1 << 31))
+    return fail(KVP_ERR_UNSUPPORTED, "%s: pool has 2^31 or more slots", fn);
+  if ((int64_t)max_blocks_per_seq * block_size > (int64_t)1 << 30)
+    return fail(KVP_ERR_UNSUPPORTED, "%s: context capacity too large", fn);
+  if (num_seqs == 0 || total_q == 0) return KVP_OK;
+  if (!q || !k || !v || !slot_mapping || !k_cache || !v_cache || !block_tables || !cu_seqlens_q ||
+      !cu_seqlens_k || !out)
+    return fail(KVP_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (!aligned16(q) || !aligned16(out) || !aligned16(k) || !aligned16(v) || !aligned16(k_cache) ||
+      !aligned16(v_cache) || q_stride_tok % 8 || out_stride_tok % 8 || kv_stride_tok % 8)
+    return fail(KVP_ERR_INVALID_ARG,
+                "%s: q, k, v, caches and out need 16-byte alignment and row strides that are "
+                "multiples of 8 elements",
+                fn);
+  int dev, *status, sms;
+  int rc = device_info(&dev, &status, &sms);
+  if (rc) return rc;
+  const int nd = num_decode_seqs, np = num_seqs - nd;
+  const int64_t tq_p = total_q - nd;  // query rows of the prefill sequences
+  // Default share of the decode rows: 7/12 of the SMs (88 of 152), the best
+  // split measured on a step of 4 chunks (3772 rows) and 128 decode rows.
+  const int dec_sms =
+      nd == 0 ? 0 : (np == 0 ? sms : (decode_sms > 0 && decode_sms < sms ? decode_sms : sms * 7 / 12));
+  // The decode rows: the last nd sequences, one query row each, the store of
+  // their new rows fused into the decode.
+  kvp::DecodePlan plan{};
+  if (nd > 0) {
+    plan = kvp::plan_decode(nd, num_heads, head_dim, max_seqlen_k, dec_sms);
+    if (!workspace || workspace_bytes < plan.total_bytes || !aligned16(workspace))
+      return fail(KVP_ERR_WORKSPACE, "%s: workspace needs %zu bytes (got %zu)", fn,
+                  plan.total_bytes, workspace_bytes);
+  }
+  // One stream, chained by programmatic dependent launches: the store of the
+  // prefill rows, the prefill on sms - dec_sms SMs (a dependent of the store;
+  // it lets its own dependents start at once), then the decode rows' split
+  // kernel on the remaining SMs (a dependent of the prefill that completes
+  // after it) and its merge.  The two halves touch disjoint rows, slots and
+  // outputs, and a kernel that follows the call on the stream sees them both
+  // complete.
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (np > 0 && tq_p > 0) {
+    cudaError_t e = kvp::launch_kv_store_narrow(k, v, kv_stride_tok, slot_mapping, tq_p, k_cache,
+                                                v_cache, num_blocks * (int64_t)block_size,
+                                                num_kv_heads * head_dim, sms - dec_sms, status, st,
+                                                true);
+    if (e != cudaSuccess) return fail_cuda(e, "attn_mixed_step: store launch");
+    const kvp::PrefillAppend app{k, v, kv_stride_tok};
+    const char* why = nullptr;
+    rc = kvp::launch_prefill(q, q_stride_tok, tq_p, k, v, kv_stride_tok, tq_p, k_cache, v_cache,
+                             num_blocks, block_size, block_tables, max_blocks_per_seq, cu_seqlens_q,
+                             cu_seqlens_k, max_seqlen_q, max_seqlen_k, np, num_heads, num_kv_heads,
+                             head_dim, softmax_scale, out, out_stride_tok, sms - dec_sms, status, st,
+                             &why, &app);
+    if (rc) return fail(rc, "%s: %s", fn, why ? why : "prefill launch failed");
+  }
+  if (nd > 0) {
+    const int64_t r0 = tq_p;
+    const kvp::DecodeAppend app{k + r0 * kv_stride_tok, v + r0 * kv_stride_tok, kv_stride_tok,
+                                kv_stride_tok, slot_mapping + r0, k_cache, v_cache};
+    const kvp::DecodeRowsOf rows{cu_seqlens_q, cu_seqlens_k, np};
+    cudaError_t e = kvp::launch_decode(q + r0 * q_stride_tok, q_stride_tok, k_cache, v_cache,
+                                       num_blocks, block_size,
+                                       block_tables + (int64_t)np * max_blocks_per_seq,
+                                       max_blocks_per_seq, nullptr, nd, num_heads, num_kv_heads,
+                                       head_dim, softmax_scale, plan, workspace,
+                                       out + r0 * out_stride_tok, out_stride_tok, status, st, &app,
+                                       &rows, np > 0 && tq_p > 0);
+    if (e != cudaSuccess) return fail_cuda(e, "attn_mixed_step: decode launch");
+  }
   return KVP_OK;
 }
 

@@ -88,7 +88,10 @@ struct DecodeArgs {
   int block_size;
   const int32_t* block_tables;
   int max_blocks;
-  const int32_t* ctx;
+  const int32_t* ctx;  // context_lens, or null: from cu_k (the decode rows of a mixed step)
+  const int32_t* cu_q;  // mixed step: cu_seqlens_q / cu_seqlens_k of the whole batch, whose
+  const int32_t* cu_k;  //   sequences cu_off .. cu_off + num_seqs - 1 are this call's rows
+  int cu_off;
   int num_seqs;
   int num_heads;
   int num_kv_heads;
@@ -120,6 +123,14 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 __device__ __forceinline__ int clamp_len(int c, int cap) { return c < 0 ? 0 : (c > cap ? cap : c); }
+
+// Context length of sequence b: context_lens[b], or, for the decode rows of a
+// mixed step, the key count of batch sequence cu_off + b (its one query row
+// is the token at position context - 1).
+__device__ __forceinline__ int seq_ctx(const DecodeArgs& a, int b) {
+  if (a.ctx) return a.ctx[b];
+  return a.cu_k[a.cu_off + b + 1] - a.cu_k[a.cu_off + b];
+}
 
 template <int D>
 __host__ __device__ constexpr size_t stage_half_bytes() {
@@ -160,7 +171,7 @@ __device__ void stream_stages(const DecodeArgs& a, const AppendArgs& app, const 
   long long pos = start, cum = cum0;
   int b = b0;
   while (ok && pos < end && b < a.num_seqs) {
-    const int L = clamp_len(a.ctx[b], cap);
+    const int L = clamp_len(seq_ctx(a, b), cap);
     if (L == 0) {
       ++b;
       continue;
@@ -270,7 +281,7 @@ __device__ void fused_store(const DecodeArgs& a, const AppendArgs& app, int lane
       if (lane == 0) record_error(a.status, KVP_ERR_DEVICE_DATA);
       continue;
     }
-    const int L = clamp_len(a.ctx[b], cap);
+    const int L = clamp_len(seq_ctx(a, b), cap);
     if (L > 0 && lane == 0) {
       const int lb = (L - 1) / a.block_size;
       const int phys = a.block_tables[(int64_t)b * a.max_blocks + lb];
@@ -299,7 +310,9 @@ __device__ void decode_producer(const DecodeArgs& a, const AppendArgs& app, cons
   // Total tokens of the batch (every CTA computes the same value).
   long long tot = 0;
   for (int i = lane; i < a.num_seqs; i += 32) {
-    const int c = a.ctx[i];
+    const int c = seq_ctx(a, i);
+    if (!a.ctx && a.cu_q[a.cu_off + i + 1] - a.cu_q[a.cu_off + i] != 1)
+      record_error(a.status, KVP_ERR_DEVICE_DATA);  // a decode row queries one token
     if (c < 0 || c > cap) record_error(a.status, KVP_ERR_DEVICE_DATA);
     tot += clamp_len(c, cap);
   }
@@ -311,7 +324,7 @@ __device__ void decode_producer(const DecodeArgs& a, const AppendArgs& app, cons
 
   // Rows of sequences with no context are zero (they read nothing).
   for (int b = blockIdx.x; b < a.num_seqs; b += P) {
-    if (clamp_len(a.ctx[b], cap) != 0) continue;
+    if (clamp_len(seq_ctx(a, b), cap) != 0) continue;
     uint4* o = reinterpret_cast<uint4*>(a.out + (int64_t)b * a.out_stride);
     for (int i = lane; i < a.num_heads * D / 8; i += 32) o[i] = make_uint4(0, 0, 0, 0);
   }
@@ -323,7 +336,7 @@ __device__ void decode_producer(const DecodeArgs& a, const AppendArgs& app, cons
     long long run = 0;
     for (int base = 0; base < a.num_seqs; base += 32) {
       const int i = base + lane;
-      const long long c = i < a.num_seqs ? clamp_len(a.ctx[i], cap) : 0;
+      const long long c = i < a.num_seqs ? clamp_len(seq_ctx(a, i), cap) : 0;
       long long incl = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -644,6 +657,10 @@ __global__ void __launch_bounds__((kBaseWarps + 1) * 32, 1)
     decode_producer<D, RS, false>(a, app, nullptr, nullptr, ringK, ringV, meta, full, empty);
   else
     decode_consumer<D, G, RS>(a, ringK, ringV, meta, full, empty, xfull, xfree, xw);
+  // Launched as a programmatic dependent (the decode rows of a mixed step,
+  // beside the prefill): do not complete before the prerequisite grid.
+  // Otherwise a no-op.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- tensor-core consumers
@@ -984,6 +1001,9 @@ __global__ void __launch_bounds__((kBaseWarps + 1) * 32, 1)
     decode_producer<D, RS, true>(a, app, &tmK, &tmV, ringK, ringV, meta, full, empty);
   else
     decode_consumer_mma<D, G, RS>(a, app, ringK, ringV, meta, full, empty, xfull, xfree, xw);
+  // As in decode_split_kernel: a programmatic dependent completes after its
+  // prerequisite grid.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // Combines the partials of every sequence that crosses a CTA boundary.
@@ -1058,15 +1078,32 @@ __global__ void __launch_bounds__(D) decode_merge_kernel(const float* __restrict
   out[(int64_t)b * out_stride + (int64_t)h * D + e] = *reinterpret_cast<const uint16_t*>(&r);
 }
 
+// Launches a split kernel, as a programmatic dependent of the stream's
+// previous kernel when pdl is set (it may then start beside that kernel).
+template <typename... Params, typename... Args>
+cudaError_t launch_split(void (*kernel)(Params...), int ctas, size_t smem, cudaStream_t stream,
+                         bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ctas);
+  cfg.blockDim = dim3((kBaseWarps + 1) * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 template <int D, int G>
 cudaError_t launch_decode_t(const DecodeArgs& a, const AppendArgs& app, int ctas,
-                            cudaStream_t stream) {
+                            cudaStream_t stream, bool pdl) {
   const size_t smem = decode_smem_bytes<D, G>(kStages);
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_split_kernel<D, G><<<ctas, (kBaseWarps + 1) * 32, smem, stream>>>(a, app);
-  e = cudaGetLastError();
+  e = launch_split(decode_split_kernel<D, G>, ctas, smem, stream, pdl, a, app);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ctas, a.num_heads);
@@ -1142,15 +1179,15 @@ cudaError_t launch_merge(const DecodeArgs& a, int D, int ctas, cudaStream_t stre
 }
 
 template <int D, int G>
-cudaError_t launch_decode_mma_t(DecodeArgs a, const AppendArgs& app, int ctas, cudaStream_t stream) {
+cudaError_t launch_decode_mma_t(DecodeArgs a, const AppendArgs& app, int ctas, cudaStream_t stream,
+                                bool pdl) {
   CUtensorMap mk, mv;
   if (!decode_maps(a, D, &mk, &mv, &a.tma_per_head)) return cudaErrorInvalidValue;
   const size_t smem = decode_mma_smem_bytes<D, G>(mma_ring_stages<D, G>());
   cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, G>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  decode_mma_kernel<D, G><<<ctas, (kBaseWarps + 1) * 32, smem, stream>>>(mk, mv, a, app);
-  e = cudaGetLastError();
+  e = launch_split(decode_mma_kernel<D, G>, ctas, smem, stream, pdl, mk, mv, a, app);
   if (e != cudaSuccess) return e;
   return launch_merge(a, D, ctas, stream);
 }
@@ -1166,11 +1203,11 @@ constexpr bool use_mma() {
 
 template <int D, int G>
 cudaError_t launch_decode_any(const DecodeArgs& a, const AppendArgs& app, int ctas,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, bool pdl) {
   if constexpr (use_mma<D, G>())
-    return launch_decode_mma_t<D, G>(a, app, ctas, stream);
+    return launch_decode_mma_t<D, G>(a, app, ctas, stream, pdl);
   else
-    return launch_decode_t<D, G>(a, app, ctas, stream);
+    return launch_decode_t<D, G>(a, app, ctas, stream, pdl);
 }
 
 }  // namespace
@@ -1186,6 +1223,7 @@ bool decode_supported(int num_heads, int num_kv_heads, int head_dim) {
 
 DecodePlan plan_decode(int num_seqs, int num_heads, int head_dim, int max_context_len,
                        int num_sms) {
+  // num_sms: the SMs the split kernel may take (one persistent CTA each).
   DecodePlan p{};
   long long upper = (long long)num_seqs * (max_context_len > 0 ? max_context_len : 0);
   long long ctas = (upper + 63) / 64;  // at least 64 tokens per CTA
@@ -1204,7 +1242,7 @@ cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k
                           int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                           float softmax_scale, const DecodePlan& plan, void* workspace,
                           uint16_t* out, int64_t out_stride, int* status, cudaStream_t stream,
-                          const DecodeAppend* app) {
+                          const DecodeAppend* app, const DecodeRowsOf* rows_of, bool pdl) {
   DecodeArgs a;
   AppendArgs ap{};
   if (app) {
@@ -1224,7 +1262,10 @@ cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k
   a.block_size = block_size;
   a.block_tables = block_tables;
   a.max_blocks = max_blocks;
-  a.ctx = ctx;
+  a.ctx = rows_of ? nullptr : ctx;
+  a.cu_q = rows_of ? rows_of->cu_q : nullptr;
+  a.cu_k = rows_of ? rows_of->cu_k : nullptr;
+  a.cu_off = rows_of ? rows_of->offset : 0;
   a.num_seqs = num_seqs;
   a.num_heads = num_heads;
   a.num_kv_heads = num_kv_heads;
@@ -1239,17 +1280,17 @@ cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k
   const int G = num_heads / num_kv_heads;
   if (head_dim == 128) {
     switch (G) {
-      case 1: return launch_decode_any<128, 1>(a, ap, plan.ctas, stream);
-      case 2: return launch_decode_any<128, 2>(a, ap, plan.ctas, stream);
-      case 4: return launch_decode_any<128, 4>(a, ap, plan.ctas, stream);
-      case 8: return launch_decode_any<128, 8>(a, ap, plan.ctas, stream);
+      case 1: return launch_decode_any<128, 1>(a, ap, plan.ctas, stream, pdl);
+      case 2: return launch_decode_any<128, 2>(a, ap, plan.ctas, stream, pdl);
+      case 4: return launch_decode_any<128, 4>(a, ap, plan.ctas, stream, pdl);
+      case 8: return launch_decode_any<128, 8>(a, ap, plan.ctas, stream, pdl);
     }
   } else if (head_dim == 64) {
     switch (G) {
-      case 1: return launch_decode_any<64, 1>(a, ap, plan.ctas, stream);
-      case 2: return launch_decode_any<64, 2>(a, ap, plan.ctas, stream);
-      case 4: return launch_decode_any<64, 4>(a, ap, plan.ctas, stream);
-      case 8: return launch_decode_any<64, 8>(a, ap, plan.ctas, stream);
+      case 1: return launch_decode_any<64, 1>(a, ap, plan.ctas, stream, pdl);
+      case 2: return launch_decode_any<64, 2>(a, ap, plan.ctas, stream, pdl);
+      case 4: return launch_decode_any<64, 4>(a, ap, plan.ctas, stream, pdl);
+      case 8: return launch_decode_any<64, 8>(a, ap, plan.ctas, stream, pdl);
     }
   }
   return cudaErrorInvalidValue;

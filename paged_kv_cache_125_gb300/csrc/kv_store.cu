@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(kNarrowThreads, 1) kv_store_narrow_kernel(
 cudaError_t launch_kv_store_narrow(const uint16_t* k, const uint16_t* v, int64_t stride,
                                    const int32_t* slots, int64_t n, uint16_t* k_cache,
                                    uint16_t* v_cache, int64_t total_slots, int row_elems,
-                                   int num_sms, int* status, cudaStream_t stream) {
+                                   int num_sms, int* status, cudaStream_t stream, bool pdl) {
   if (n == 0) return cudaSuccess;
   int64_t grid = (n + kNarrowThreads / 32 - 1) / (kNarrowThreads / 32);
   const int64_t cap = num_sms / 2 > 0 ? num_sms / 2 : 1;
@@ -150,7 +150,7 @@ cudaError_t launch_kv_store_narrow(const uint16_t* k, const uint16_t* v, int64_t
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kv_store_narrow_kernel, k, v, stride, slots, n, k_cache, v_cache,
                             total_slots, row_elems, status);
 }

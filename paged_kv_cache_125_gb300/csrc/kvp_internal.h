@@ -34,10 +34,12 @@ cudaError_t launch_kv_store(const uint16_t* k, const uint16_t* v, int64_t k_stri
 // The store of attn_prefill_varlen_append (16-byte aligned rows; k and v
 // share a row stride): at most num_sms / 2 CTAs of 1024 threads, which let
 // the prefill launched as their programmatic dependent start on the others.
+// pdl: launched itself as a programmatic dependent of the stream's previous
+// kernel (it waits for that kernel before touching memory).
 cudaError_t launch_kv_store_narrow(const uint16_t* k, const uint16_t* v, int64_t stride,
                                    const int32_t* slots, int64_t n, uint16_t* k_cache,
                                    uint16_t* v_cache, int64_t total_slots, int row_elems,
-                                   int num_sms, int* status, cudaStream_t stream);
+                                   int num_sms, int* status, cudaStream_t stream, bool pdl);
 
 // copy_blocks.cu
 cudaError_t launch_copy_blocks(uint16_t* cache, int64_t num_planes, int64_t plane_stride,
@@ -64,13 +66,24 @@ struct DecodeAppend {
   uint16_t* k_cache;
   uint16_t* v_cache;
 };
+// The decode rows of a mixed step: sequence b of the call is sequence
+// offset + b of a varlen batch; its context length is cu_k[offset + b + 1] -
+// cu_k[offset + b] (context_lens unused) and its q_len (cu_q) must be 1.
+// pdl: the split kernel is launched as a programmatic dependent of the
+// stream's previous kernel (it starts beside it and completes after it).
+struct DecodeRowsOf {
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  int offset;
+};
 cudaError_t launch_decode(const uint16_t* q, int64_t q_stride, const uint16_t* k_cache,
                           const uint16_t* v_cache, int64_t num_blocks, int block_size,
                           const int32_t* block_tables, int max_blocks, const int32_t* ctx,
                           int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                           float softmax_scale, const DecodePlan& plan, void* workspace,
                           uint16_t* out, int64_t out_stride, int* status, cudaStream_t stream,
-                          const DecodeAppend* app = nullptr);
+                          const DecodeAppend* app = nullptr, const DecodeRowsOf* rows_of = nullptr,
+                          bool pdl = false);
 
 // prefill.cu: cuTensorMapEncodeTiled (a PFN_cuTensorMapEncodeTiled_v12000), or
 // null if the driver does not provide it.
