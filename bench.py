@@ -53,8 +53,8 @@ N_SETS = 4
 TRAFFIC = {
     # decode B64 workload (one input set), one ncu --set full capture of the split kernel
     "decode": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu",
-               "sha256": "6714505f9679338af3c493ee75631c3e57932872a7e33bd5287ac720069b22d3",
-               "bytes": 569288960 + 4451072},
+               "sha256": "07f434c766015d559ae0affb2f61e9797e9003a251cbb795c3e28b4c04ea3955",
+               "bytes": 569347584 + 3980544},
     # decode B512 mix: one capture of the tensor-core split kernel on 128 of the sequences
     # (1790.12 MB for 1778.58 MB algorithmic), scaled to the 512-sequence launch by its algorithmic
     # bytes (7062.70 MB)
@@ -66,8 +66,11 @@ TRAFFIC = {
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
                 "sha256": "dee9572eec0f1aab8bcb4bc5fb5d62b841c14ca619dc101da703f29f6e14dcba",
                 "bytes": 111434496 + 33398272},
-    # the prefill workload's suffix store (8150 rows), one ncu capture
-    "kv_store": {"file": "paged_kv_cache_125_gb300/csrc/kv_store.cu", "sha256": None, "bytes": None},
+    # the prefill workload's suffix store (8150 rows), one ncu capture of kv_store_kernel
+    # (SpeedOfLight + MemoryWorkloadAnalysis: dram__bytes.sum.per_second x gpu__time_duration.sum)
+    "kv_store": {"file": "paged_kv_cache_125_gb300/csrc/kv_store.cu",
+                 "sha256": "3de4572fdae061866219311055c3a52252d20b51b0cd3367ae6c4c0e416b6024",
+                 "bytes": 34464000},
 }
 
 

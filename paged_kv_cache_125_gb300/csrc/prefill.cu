@@ -1107,7 +1107,11 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
     return KVP_ERR_UNSUPPORTED;
   }
   const int grid = (int)(items < num_sms ? items : num_sms);
-  a.dynamic = (long long)a.max_pairs * num_seqs <= kMaxPairs ? 1 : 0;
+  // With at most one item per CTA (small steps: items <= grid), CTA x takes
+  // item x and nothing is scheduled: no cost sort, no counter, cu_seqlens read
+  // where the item is decoded.
+  const bool one_each = items <= grid;
+  a.dynamic = !one_each && (long long)a.max_pairs * num_seqs <= kMaxPairs ? 1 : 0;
   a.qslot = nullptr;
   a.qdone = nullptr;
   a.epoch = 0;
@@ -1122,7 +1126,7 @@ int launch_prefill(const uint16_t* q, int64_t q_stride, int64_t total_q, const u
     a.qdone = qs.done;
     a.epoch = qs.epoch;
   }
-  a.cu_in_smem = num_seqs + 1 <= kCuCap ? 1 : 0;
+  a.cu_in_smem = !one_each && num_seqs + 1 <= kCuCap ? 1 : 0;
   cudaError_t e = head_dim == 128 ? launch_t<128>(mq, mk, mv, mkn, mvn, a, grid, stream)
                                   : launch_t<64>(mq, mk, mv, mkn, mvn, a, grid, stream);
   if (e != cudaSuccess) {

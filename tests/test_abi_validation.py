@@ -184,3 +184,36 @@ def test_prefill_append_validation(lib):
     for name in ("q", "k", "v", "kc", "vc", "out"):
         assert _prefill_append(lib, **{name: MIS}) == INVALID and "16-byte" in _err(lib), name
     assert _prefill_append(lib, kv_stride=8 * 128 + 4) == INVALID and "multiples of 8" in _err(lib)
+
+
+def _mixed(lib, **kw):
+    a = dict(q=A, q_stride=32 * 128, tq=20, k=A, v=A, kv_stride=8 * 128, slots=A, kc=A, vc=A, nb=64,
+             bs=256, bt=A, mb=16, cq=A, ck=A, mq=16, mk=4096, b=5, nd=4, dsms=0, hq=32, hkv=8, d=128,
+             ws=A, wsb=1 << 20, out=A, out_stride=32 * 128)
+    a.update(kw)
+    return lib.attn_mixed_step(a["q"], a["q_stride"], a["tq"], a["k"], a["v"], a["kv_stride"], a["slots"],
+                               a["kc"], a["vc"], a["nb"], a["bs"], a["bt"], a["mb"], a["cq"], a["ck"],
+                               a["mq"], a["mk"], a["b"], a["nd"], a["dsms"], a["hq"], a["hkv"], a["d"],
+                               0.088, a["ws"], a["wsb"], a["out"], a["out_stride"], None)
+
+
+def test_mixed_step_validation(lib):
+    assert _mixed(lib, b=0, nd=0) == OK               # no sequences: a no-op
+    assert _mixed(lib, tq=0, nd=0) == OK              # no query rows: a no-op
+    assert _mixed(lib, nd=6) == INVALID and "bad sizes" in _err(lib)        # more decode rows than seqs
+    assert _mixed(lib, nd=-1) == INVALID and "attn_mixed_step" in _err(lib)
+    assert _mixed(lib, dsms=-1) == INVALID
+    assert _mixed(lib, tq=3) == INVALID                # fewer query rows than decode rows
+    assert _mixed(lib, tq=1 << 31) == INVALID
+    assert _mixed(lib, hq=24) == UNSUPPORTED and "unsupported" in _err(lib)
+    assert _mixed(lib, bs=48) == UNSUPPORTED
+    assert _mixed(lib, hq=8, hkv=8, d=96) == UNSUPPORTED   # head_dim the decode does not take
+    assert _mixed(lib, out_stride=32 * 128 - 8) == INVALID and "stride" in _err(lib)
+    assert _mixed(lib, nb=0) == INVALID and "num_blocks" in _err(lib)
+    assert _mixed(lib, nb=1 << 24) == UNSUPPORTED and "2^31" in _err(lib)
+    assert _mixed(lib, mb=1 << 20, bs=4096, nb=16) == UNSUPPORTED and "capacity" in _err(lib)
+    for name in ("q", "k", "v", "slots", "kc", "vc", "bt", "cq", "ck", "out"):
+        assert _mixed(lib, **{name: None}) == INVALID and "null" in _err(lib), name
+    for name in ("q", "k", "v", "kc", "vc", "out"):
+        assert _mixed(lib, **{name: MIS}) == INVALID and "16-byte" in _err(lib), name
+    assert _mixed(lib, q_stride=32 * 128 + 4) == INVALID and "multiples of 8" in _err(lib)
