@@ -56,11 +56,11 @@ TRAFFIC = {
                "sha256": "07f434c766015d559ae0affb2f61e9797e9003a251cbb795c3e28b4c04ea3955",
                "bytes": 569347584 + 3980544},
     # decode B512 mix: one capture of the tensor-core split kernel on 128 of the sequences
-    # (1790.12 MB for 1778.58 MB algorithmic), scaled to the 512-sequence launch by its algorithmic
+    # (1789.71 MB for 1778.58 MB algorithmic), scaled to the 512-sequence launch by its algorithmic
     # bytes (7062.70 MB)
     "decode_b512": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu",
-                    "sha256": "ad1b2d380ba008f2599e85310180784f5339cf77cce8bec90c20afe4f31dda21",
-                    "bytes": 7108547269},
+                    "sha256": "07f434c766015d559ae0affb2f61e9797e9003a251cbb795c3e28b4c04ea3955",
+                    "bytes": 7106903694},
     # prefill workload (8 prompts, 32/8/128), one ncu --set full capture of the prefill kernel of
     # attn_prefill_varlen_append
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
