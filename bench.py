@@ -64,8 +64,8 @@ TRAFFIC = {
     # prefill workload (8 prompts, 32/8/128), one ncu --set full capture of the prefill kernel of
     # attn_prefill_varlen_append
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
-                "sha256": "dee9572eec0f1aab8bcb4bc5fb5d62b841c14ca619dc101da703f29f6e14dcba",
-                "bytes": 111434496 + 33398272},
+                "sha256": "87f871db8ebb10db8884dfb6f61e8fbd782b1ab78e6e3c724783916fafdec3e9",
+                "bytes": 111977728 + 33583360},
     # the prefill workload's suffix store (8150 rows), one ncu capture of kv_store_kernel
     # (SpeedOfLight + MemoryWorkloadAnalysis: dram__bytes.sum.per_second x gpu__time_duration.sum)
     "kv_store": {"file": "paged_kv_cache_125_gb300/csrc/kv_store.cu",
@@ -648,7 +648,7 @@ def measure_mixed(args, kvp, W, dev, stream, world, peaks):
     3772 tokens, + 128 decode rows, 32/8/128), launched eagerly over 2 input
     sets in rotation.  The step is attn_mixed_step: the chunks through the
     fused store + prefill on part of the SMs, the decode rows through the
-    decode kernel (store fused) on the others (7/12 of the SMs by default),
+    decode kernel (store fused) on the others (5/8 of the SMs by default),
     side by side; a short sweep of
     the decode rows' SM share, and the same step as one
     attn_prefill_varlen_append call (decode rows as q_len-1 sequences of the
@@ -676,7 +676,7 @@ def measure_mixed(args, kvp, W, dev, stream, world, peaks):
     ms_step, _, win = timed_loop_eager(no_call, mixed, msets, steps, args.warmup, world, call_events=False)
     _, ms_call, _ = timed_loop_eager(no_call, mixed, msets, steps, args.warmup, world)
     sweep = {}
-    for dsms in (64, 76, 100, 112):
+    for dsms in (76, 88, 96, 100):
         t, _, _ = timed_loop_eager(no_call, lambda s_: mixed(s_, dsms), msets, steps, 3, world,
                                    call_events=False)
         sweep[str(dsms)] = round(nbytes / (t * 1e-3) / 1e9, 1)
@@ -691,7 +691,7 @@ def measure_mixed(args, kvp, W, dev, stream, world, peaks):
             "line": {"workload": wm.description, "value": round(nbytes / (ms_step * 1e-3) / 1e9, 1),
                      "unit": "GB/s", "ms_per_step": round(ms_step, 4), "steps": steps,
                      "step": "attn_mixed_step: chunks (store + prefill) beside the 128 decode rows "
-                             "(decode, store fused) on 88 of the 152 SMs, one stream, chained by programmatic "
+                             "(decode, store fused) on 95 of the 152 SMs, one stream, chained by programmatic "
                              "dependent launches",
                      "roofline": {"kernel": "attn_mixed_step (store + prefill | decode)", "bound": "hbm",
                                   "achieved": round(gbs_call, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -438,10 +438,11 @@ int attn_mixed_step(const kvp_bf16* q, int64_t q_stride_tok, int64_t total_q, co
   if (rc) return rc;
   const int nd = num_decode_seqs, np = num_seqs - nd;
   const int64_t tq_p = total_q - nd;  // query rows of the prefill sequences
-  // Default share of the decode rows: 7/12 of the SMs (88 of 152), the best
-  // split measured on a step of 4 chunks (3772 rows) and 128 decode rows.
+  // Default share of the decode rows: 5/8 of the SMs (95 of 152), near the
+  // best split measured on a step of 4 chunks (3772 rows) and 128 decode rows
+  // (past ~97 of 152 the chunks become the longer half).
   const int dec_sms =
-      nd == 0 ? 0 : (np == 0 ? sms : (decode_sms > 0 && decode_sms < sms ? decode_sms : sms * 7 / 12));
+      nd == 0 ? 0 : (np == 0 ? sms : (decode_sms > 0 && decode_sms < sms ? decode_sms : sms * 5 / 8));
   // The decode rows: the last nd sequences, one query row each, the store of
   // their new rows fused into the decode.
   kvp::DecodePlan plan{};
