@@ -865,7 +865,8 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
     with an empty launch queue)."""
     import torch
     from paged_kv_cache_125_gb300 import engine_trace as E
-    from paged_kv_cache_125_gb300.engine_replay import EngineReplay, decode_bytes, prefill_flops
+    from paged_kv_cache_125_gb300.engine_replay import (EngineReplay, decode_bytes, prefill_flops,
+                                                        prefill_layer_bytes)
     layers, hq, hkv, d, bs, nb = 28, 16, 8, 128, 256, 768
     torch.cuda.empty_cache()
     reqs = E.make_requests(256, (100, 1024), (100, 1024))
@@ -881,12 +882,14 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
             k = torch.randn((layers, n, hkv, d), generator=gq, device=dev).to(torch.bfloat16)
             v = torch.randn((layers, n, hkv, d), generator=gq, device=dev).to(torch.bfloat16)
             work = prefill_flops(st.meta, d, hq)
+            pbytes = prefill_layer_bytes(st.meta, hq, hkv, d)
         else:  # every layer's new rows, straight into the graph's buffers
             q, k, v = eng.decode_inputs(st)
             q.copy_(torch.randn(q.shape, generator=gq, device=dev))
             k.copy_(torch.randn(k.shape, generator=gq, device=dev))
             v.copy_(torch.randn(v.shape, generator=gq, device=dev))
             work = decode_bytes(st.meta, n, hq, hkv, d, bs)
+            pbytes = 0
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if st.is_prefill:
             # Drain the launch queue (the host runs steps ahead of the device,
@@ -901,7 +904,7 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
         eng.launch(st, q, k, v)
         host_us = (time.perf_counter() - h0) * 1e6
         b.record()
-        recs.append((st.is_prefill, work * layers, a, b, n, len(st.seq_ids), host_us))
+        recs.append((st.is_prefill, work * layers, a, b, n, len(st.seq_ids), host_us, pbytes * layers))
         eng.commit(st, [(7 * i + n) % 151936 for i in st.seq_ids])
         del q, k, v
     torch.cuda.synchronize()
@@ -912,24 +915,33 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
     dec_work = sum(w_ for p_, w_, *_ in recs if not p_)
     pre_work = sum(w_ for p_, w_, *_ in recs if p_)
     n_dec = sum(1 for r in recs if not r[0])
-    # prefill steps by query tokens
+    # prefill steps by query tokens; each step's roofline time is the larger of its algorithmic
+    # bytes at the measured copy bandwidth and its FLOPs at the measured bf16 burst peak
     groups = {}
-    for p_, w_, a, b, n, ns, host_us in recs:
+    roof_ms = 0.0
+    for p_, w_, a, b, n, ns, host_us, pb in recs:
         if not p_:
             continue
         key = ">=8192 tokens" if n >= 8192 else ("1024-8191 tokens" if n >= 1024 else "<1024 tokens")
         g = groups.setdefault(key, {"steps": 0, "tokens": 0, "seqs": 0, "ms": 0.0, "tflop": 0.0,
-                                    "host_ms": 0.0})
+                                    "gbytes": 0.0, "roof_ms": 0.0, "host_ms": 0.0})
+        r_ms = max(pb / (peaks["hbm_gbs"] * 1e9), w_ / (peaks["bf16_tflops"] * 1e12)) * 1e3
+        roof_ms += r_ms
         g["steps"] += 1
         g["tokens"] += n
         g["seqs"] += ns
         g["ms"] += a.elapsed_time(b)
         g["tflop"] += w_ / 1e12
+        g["gbytes"] += pb / 1e9
+        g["roof_ms"] += r_ms
         g["host_ms"] += host_us / 1e3
     for g in groups.values():
         g["ms"] = round(g["ms"], 3)
         g["tflop"] = round(g["tflop"], 4)
+        g["gbytes"] = round(g["gbytes"], 3)
         g["us_per_layer_call"] = round(g["ms"] * 1e3 / (g["steps"] * layers), 2)
+        g["roofline_us_per_layer_call"] = round(g["roof_ms"] * 1e3 / (g["steps"] * layers), 2)
+        g["frac_of_roofline"] = round(g.pop("roof_ms") / g["ms"], 4)
         g["host_us_per_layer_call"] = round(g.pop("host_ms") * 1e3 / (g["steps"] * layers), 2)
         g["tflops"] = round(g["tflop"] / (g["ms"] * 1e-3), 1)
     preempt = eng.num_preemptions
@@ -946,6 +958,11 @@ def measure_trace(args, kvp, dev, stream, world, peaks):
                                 "frac_of_hbm": round(dec_gbs / peaks["hbm_gbs"], 4)},
                      "prefill": {"value": round(pre_tf, 2), "unit": "TFLOP/s", "ms": round(pre_ms, 2),
                                  "frac_of_bf16_burst": round(pre_tf / peaks["bf16_tflops"], 4),
+                                 "frac_of_roofline": round(roof_ms / pre_ms, 4),
+                                 "roofline": "per step: max(algorithmic bytes / measured copy bandwidth, "
+                                             "causal FLOPs / measured bf16 burst peak); bytes per layer "
+                                             "call: q, the new K/V rows read and stored, the output, and "
+                                             "the cached prefix's K/V",
                                  "by_query_tokens": groups},
                      "how": "EngineReplay: event pair around each step's launch of 28 layers (prefill: "
                             "attn_prefill_varlen_append per layer, eager; decode: one copy of the "

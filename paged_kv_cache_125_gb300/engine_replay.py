@@ -152,6 +152,17 @@ def prefill_flops(meta, head_dim: int, num_heads: int) -> int:
     return 4 * head_dim * num_heads * int((ql * (kl - ql) + ql * (ql + 1) // 2).sum())
 
 
+def prefill_layer_bytes(meta, num_heads: int, num_kv_heads: int, head_dim: int) -> int:
+    """Algorithmic bytes of one prefill layer call (store fused): q read and
+    the output written (2 * Hq * d bf16 per query row), the new K/V rows read
+    and stored (4 * Hkv * d bf16 per query row), and the cached prefix's K
+    and V read once per kv head (2 * Hkv * d bf16 per cached key)."""
+    ql = (meta.cu_seqlens_q[1:] - meta.cu_seqlens_q[:-1]).long()
+    kl = (meta.cu_seqlens_k[1:] - meta.cu_seqlens_k[:-1]).long()
+    rows, cached = int(ql.sum()), int((kl - ql).sum())
+    return rows * (2 * num_heads + 4 * num_kv_heads) * head_dim * 2 + cached * 2 * num_kv_heads * head_dim * 2
+
+
 def decode_bytes(meta, num_new: int, num_heads: int, num_kv_heads: int, head_dim: int,
                  block_size: int) -> int:
     """Algorithmic bytes of one decode layer call (store fused): the new rows
