@@ -441,8 +441,9 @@ int attn_mixed_step(const kvp_bf16* q, int64_t q_stride_tok, int64_t total_q, co
   // Default share of the decode rows: 5/8 of the SMs (95 of 152), near the
   // best split measured on a step of 4 chunks (3772 rows) and 128 decode rows
   // (past ~97 of 152 the chunks become the longer half).
+  const bool chunks = np > 0 && tq_p > 0;  // prefill rows to run beside the decode rows
   const int dec_sms =
-      nd == 0 ? 0 : (np == 0 ? sms : (decode_sms > 0 && decode_sms < sms ? decode_sms : sms * 5 / 8));
+      nd == 0 ? 0 : (!chunks ? sms : (decode_sms > 0 && decode_sms < sms ? decode_sms : sms * 5 / 8));
   // The decode rows: the last nd sequences, one query row each, the store of
   // their new rows fused into the decode.
   kvp::DecodePlan plan{};
@@ -460,7 +461,7 @@ int attn_mixed_step(const kvp_bf16* q, int64_t q_stride_tok, int64_t total_q, co
   // outputs, and a kernel that follows the call on the stream sees them both
   // complete.
   const cudaStream_t st = (cudaStream_t)stream;
-  if (np > 0 && tq_p > 0) {
+  if (chunks) {
     cudaError_t e = kvp::launch_kv_store_narrow(k, v, kv_stride_tok, slot_mapping, tq_p, k_cache,
                                                 v_cache, num_blocks * (int64_t)block_size,
                                                 num_kv_heads * head_dim, sms - dec_sms, status, st,
@@ -486,7 +487,7 @@ int attn_mixed_step(const kvp_bf16* q, int64_t q_stride_tok, int64_t total_q, co
                                        max_blocks_per_seq, nullptr, nd, num_heads, num_kv_heads,
                                        head_dim, softmax_scale, plan, workspace,
                                        out + r0 * out_stride_tok, out_stride_tok, status, st, &app,
-                                       &rows, np > 0 && tq_p > 0);
+                                       &rows, chunks);
     if (e != cudaSuccess) return fail_cuda(e, "attn_mixed_step: decode launch");
   }
   return KVP_OK;

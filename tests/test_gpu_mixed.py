@@ -95,10 +95,10 @@ def test_mixed_step_one_kind_of_rows(which):
 
 def test_mixed_step_full_size_sampled_and_graph_replay():
     """The bench's mixed step (4 chunks of a 32/8/128 model + 128 decode rows)
-    through attn_mixed_step, eager and as a CUDA-graph replay (the fork and
-    join onto the library's second stream inside the capture): every decode
-    row and every 5th chunk row against the oracle, caches bit-exact, the
-    replay bit-identical to the eager call."""
+    through attn_mixed_step, eager and as a CUDA-graph replay (the chain of
+    programmatic dependent launches captured as one graph): every decode row
+    and every 5th chunk row against the oracle, caches bit-exact, the replay
+    bit-identical to the eager call."""
     import paged_kv_cache_125_gb300 as kvp
     from parity import gpu_pool
     w = W.mixed_step_workload()
