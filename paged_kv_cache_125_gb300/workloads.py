@@ -335,7 +335,7 @@ def mixed_step_workload(device="cpu") -> Workload:
     need = sum(num_blocks_for(L, 256) for L, _ in chunks) + sum(num_blocks_for(L, 256) for L in dec)
     return mixed_workload("mixed_chunks_decode", chunks, dec, 32, 8, 128, 256, need + 64, device,
                           description="mixed: 4 prefill chunks (3772 tokens) + 128 decode rows "
-                                      "ctx U[512,4096], 32/8/128 bs256, one varlen paged launch")
+                                      "ctx U[512,4096], 32/8/128 bs256")
 
 
 # ---------------------------------------------------------------------------
