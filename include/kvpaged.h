@@ -251,7 +251,9 @@ int attn_prefill_varlen_append(const kvp_bf16 *q, int64_t q_stride_tok, int64_t 
  *                    its slot_mapping entry must be the slot of its position
  *                    k_len - 1 (as attn_decode_paged_append requires)
  *   decode_sms       SMs given to the decode rows while the chunks run on the
- *                    others (0 = 5/8 of the device's SMs, 95 of 152)
+ *                    others (0, or a value not below the device's SM count:
+ *                    5/8 of the SMs, 95 of 152); all SMs when no chunk has
+ *                    query rows
  *   workspace        as attn_decode_paged, for the decode rows: at least
  *                    attn_decode_workspace_size(num_decode_seqs, num_heads,
  *                    head_dim, max_seqlen_k, block_size) bytes
