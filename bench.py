@@ -66,6 +66,10 @@ TRAFFIC = {
     "prefill": {"file": "paged_kv_cache_125_gb300/csrc/prefill.cu",
                 "sha256": "87f871db8ebb10db8884dfb6f61e8fbd782b1ab78e6e3c724783916fafdec3e9",
                 "bytes": 111977728 + 33583360},
+    # decode 64/8/128 on the decode B64 batch, one ncu --set full capture of the split kernel
+    "decode_group8": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu",
+                      "sha256": "07f434c766015d559ae0affb2f61e9797e9003a251cbb795c3e28b4c04ea3955",
+                      "bytes": 576161024 + 5634304},
     # the prefill workload's suffix store (8150 rows), one ncu capture of kv_store_kernel
     # (SpeedOfLight + MemoryWorkloadAnalysis: dram__bytes.sum.per_second x gpu__time_duration.sum)
     "kv_store": {"file": "paged_kv_cache_125_gb300/csrc/kv_store.cu",
@@ -87,7 +91,7 @@ def parse_args():
     p.add_argument("--no-copy-blocks", action="store_true")
     p.add_argument("--no-large", action="store_true", help="skip the 150 GB decode B512 line")
     p.add_argument("--no-trace", action="store_true", help="skip the engine-trace replay line")
-    p.add_argument("--only", choices=["decode", "prefill", "decode_b512"], default=None,
+    p.add_argument("--only", choices=["decode", "prefill", "decode_b512", "decode_group8"], default=None,
                    help="run one part only (profiling); the JSON line then carries that part")
     p.add_argument("--b512-batch", type=int, default=512,
                    help="sequences of the decode B512 line (a smaller batch profiles the same kernel)")
@@ -844,7 +848,7 @@ def measure_decode_group8(args, kvp, W, dev, stream, world, peaks):
                      "roofline": {"kernel": "attn_decode_paged_append (store + split + merge)",
                                   "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                                   "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                                  "traffic": None, "algorithmic_bytes": store_b + dec_b,
+                                  "traffic": traffic_for("decode_group8"), "algorithmic_bytes": store_b + dec_b,
                                   "peak_source": peaks["source"], "ms_per_launch": round(ms_call, 5)}}}
 
 
@@ -1083,6 +1087,13 @@ def run_ours(args, rank, world, local):
     time.sleep(0.3)
     windows = []
     dec = pre = None
+    if args.only == "decode_group8":  # profiling run of the 64/8/128 decode line only
+        g8 = measure_decode_group8(args, kvp, W, dev, stream, world, peaks)
+        clocks = sampler.stop([g8["window"]])
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "only": "decode_group8", "clocks": clocks,
+                              "decode_group8": g8["line"]}), flush=True)
+        return
     if args.only == "decode_b512":  # profiling run of the large-batch decode line only
         dl = measure_decode_large(args, kvp, W, dev, stream, world, peaks)
         clocks = sampler.stop([dl["window"]] if dl["window"] else [])
