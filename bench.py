@@ -70,6 +70,19 @@ TRAFFIC = {
     "decode_group8": {"file": "paged_kv_cache_125_gb300/csrc/decode.cu",
                       "sha256": "07f434c766015d559ae0affb2f61e9797e9003a251cbb795c3e28b4c04ea3955",
                       "bytes": 576161024 + 5634304},
+    # the mixed step (one attn_mixed_step call): dram bytes of its four kernels (narrow store,
+    # prefill, tensor-core decode, merge) from one ncu --metrics capture, summed
+    "mixed": {"file": ["paged_kv_cache_125_gb300/csrc/api.cu", "paged_kv_cache_125_gb300/csrc/prefill.cu",
+                       "paged_kv_cache_125_gb300/csrc/decode.cu", "paged_kv_cache_125_gb300/csrc/kv_store.cu"],
+              "sha256": ["67530d107bbd4d9366bf0e741036ab01295e5defadb3a6051ddf6a63b3bea151",
+                         "87f871db8ebb10db8884dfb6f61e8fbd782b1ab78e6e3c724783916fafdec3e9",
+                         "07f434c766015d559ae0affb2f61e9797e9003a251cbb795c3e28b4c04ea3955",
+                         "3de4572fdae061866219311055c3a52252d20b51b0cd3367ae6c4c0e416b6024"],
+              "bytes": 1280745472},
+    # kv_copy_blocks on the 64-pair, 56-plane call, one ncu --metrics capture
+    "copy_blocks": {"file": "paged_kv_cache_125_gb300/csrc/copy_blocks.cu",
+                    "sha256": "4257c5bb2346e1bde3299c7f093b29e7939976617646de065c32796c7035dea2",
+                    "bytes": 1859943680 + 1831985920},
     # the prefill workload's suffix store (8150 rows), one ncu capture of kv_store_kernel
     # (SpeedOfLight + MemoryWorkloadAnalysis: dram__bytes.sum.per_second x gpu__time_duration.sum)
     "kv_store": {"file": "paged_kv_cache_125_gb300/csrc/kv_store.cu",
@@ -91,7 +104,8 @@ def parse_args():
     p.add_argument("--no-copy-blocks", action="store_true")
     p.add_argument("--no-large", action="store_true", help="skip the 150 GB decode B512 line")
     p.add_argument("--no-trace", action="store_true", help="skip the engine-trace replay line")
-    p.add_argument("--only", choices=["decode", "prefill", "decode_b512", "decode_group8"], default=None,
+    p.add_argument("--only", choices=["decode", "prefill", "decode_b512", "decode_group8", "mixed",
+                                      "copy_blocks"], default=None,
                    help="run one part only (profiling); the JSON line then carries that part")
     p.add_argument("--b512-batch", type=int, default=512,
                    help="sequences of the decode B512 line (a smaller batch profiles the same kernel)")
@@ -119,11 +133,16 @@ def load_peaks():
 
 
 def traffic_for(name):
+    """The entry's bytes while every source it was captured from is unchanged, else None."""
     t = TRAFFIC[name]
     if t["bytes"] is None or t["sha256"] is None:
         return None
-    src = open(os.path.join(ROOT, t["file"]), "rb").read()
-    return t["bytes"] if hashlib.sha256(src).hexdigest() == t["sha256"] else None
+    files = t["file"] if isinstance(t["file"], list) else [t["file"]]
+    shas = t["sha256"] if isinstance(t["sha256"], list) else [t["sha256"]]
+    for f, sha in zip(files, shas):
+        if hashlib.sha256(open(os.path.join(ROOT, f), "rb").read()).hexdigest() != sha:
+            return None
+    return t["bytes"]
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -699,7 +718,7 @@ def measure_mixed(args, kvp, W, dev, stream, world, peaks):
                              "dependent launches",
                      "roofline": {"kernel": "attn_mixed_step (store + prefill | decode)", "bound": "hbm",
                                   "achieved": round(gbs_call, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                  "frac": round(gbs_call / peaks["hbm_gbs"], 4), "traffic": None,
+                                  "frac": round(gbs_call / peaks["hbm_gbs"], 4), "traffic": traffic_for("mixed"),
                                   "algorithmic_bytes": nbytes, "peak_source": peaks["source"],
                                   "ms_per_launch": round(ms_call, 5),
                                   "tensor": {"achieved_tflops": round(tf_call, 1),
@@ -1065,7 +1084,7 @@ def measure_copy_blocks(args, kvp, dev, stream, world, peaks):
                      "steps": steps,
                      "roofline": {"kernel": "kv_copy_blocks", "bound": "hbm", "achieved": round(achieved, 1),
                                   "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                                  "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                                  "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic_for("copy_blocks"),
                                   "algorithmic_bytes": step_bytes, "peak_source": peaks["source"],
                                   "ms_per_launch": round(ms, 5)}}}
 
@@ -1087,19 +1106,16 @@ def run_ours(args, rank, world, local):
     time.sleep(0.3)
     windows = []
     dec = pre = None
-    if args.only == "decode_group8":  # profiling run of the 64/8/128 decode line only
-        g8 = measure_decode_group8(args, kvp, W, dev, stream, world, peaks)
-        clocks = sampler.stop([g8["window"]])
+    single = {"decode_b512": lambda: measure_decode_large(args, kvp, W, dev, stream, world, peaks),
+              "decode_group8": lambda: measure_decode_group8(args, kvp, W, dev, stream, world, peaks),
+              "mixed": lambda: measure_mixed(args, kvp, W, dev, stream, world, peaks),
+              "copy_blocks": lambda: measure_copy_blocks(args, kvp, dev, stream, world, peaks)}
+    if args.only in single:  # profiling run of one line only
+        r = single[args.only]()
+        clocks = sampler.stop([r["window"]] if r["window"] else [])
         if rank == 0:
-            print(json.dumps({"metric": METRIC, "only": "decode_group8", "clocks": clocks,
-                              "decode_group8": g8["line"]}), flush=True)
-        return
-    if args.only == "decode_b512":  # profiling run of the large-batch decode line only
-        dl = measure_decode_large(args, kvp, W, dev, stream, world, peaks)
-        clocks = sampler.stop([dl["window"]] if dl["window"] else [])
-        if rank == 0:
-            print(json.dumps({"metric": METRIC, "only": "decode_b512", "clocks": clocks,
-                              "decode_b512": dl["line"]}), flush=True)
+            print(json.dumps({"metric": METRIC, "only": args.only, "clocks": clocks,
+                              args.only: r["line"]}), flush=True)
         return
     if args.only != "prefill":
         dec = measure_decode(args, kvp, W, dev, stream, world, peaks)
