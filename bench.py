@@ -105,7 +105,7 @@ def parse_args():
     p.add_argument("--no-large", action="store_true", help="skip the 150 GB decode B512 line")
     p.add_argument("--no-trace", action="store_true", help="skip the engine-trace replay line")
     p.add_argument("--only", choices=["decode", "prefill", "decode_b512", "decode_group8", "mixed",
-                                      "copy_blocks", "decode_bucketed"], default=None,
+                                      "copy_blocks", "decode_bucketed", "engine_trace"], default=None,
                    help="run one part only (profiling); the JSON line then carries that part")
     p.add_argument("--b512-batch", type=int, default=512,
                    help="sequences of the decode B512 line (a smaller batch profiles the same kernel)")
@@ -1110,7 +1110,8 @@ def run_ours(args, rank, world, local):
               "decode_group8": lambda: measure_decode_group8(args, kvp, W, dev, stream, world, peaks),
               "mixed": lambda: measure_mixed(args, kvp, W, dev, stream, world, peaks),
               "copy_blocks": lambda: measure_copy_blocks(args, kvp, dev, stream, world, peaks),
-              "decode_bucketed": lambda: measure_bucketed(args, kvp, W, dev, stream, world, peaks)}
+              "decode_bucketed": lambda: measure_bucketed(args, kvp, W, dev, stream, world, peaks),
+              "engine_trace": lambda: measure_trace(args, kvp, dev, stream, world, peaks)}
     if args.only in single:  # profiling run of one line only
         r = single[args.only]()
         clocks = sampler.stop([r["window"]] if r["window"] else [])
